@@ -1,0 +1,55 @@
+"""The oracle's pins catch planted mistakes.
+
+Each case compiles a copy of the oracle source with one plausible mistake
+(a flipped sign, a dropped term, a wrong tie order, a transposed operand)
+and checks that at least one pin from ``test_oracle_pins`` fails on it.
+The mistakes are planted in the CPU oracle only.
+"""
+
+import os
+
+import pytest
+
+import tests.test_oracle_pins as P
+
+MUTATIONS = {
+    "residual sign flipped": ("std::max(0.0, p[y] - q[y])", "std::max(0.0, q[y] - p[y])"),
+    "accept ratio transposed": ("std::min(1.0, px / qx)", "std::min(1.0, qx / px)"),
+    "saguaro factor on the wrong set": ("for (int y : S) qp[y] = C * q[y];",
+                                        "for (int y : S) qp[y] = q[y] / C;"),
+    "saguaro not renormalised": ("for (auto& v : qp) v /= total;", ""),
+    "top-F ties to the higher index": ("(z[a] == z[b] && a < b)", "(z[a] == z[b] && a > b)"),
+    "inverse CDF not strict": ("if (cum > thr) {", "if (cum >= thr) {"),
+    "temperature dropped": ("std::exp((z[y] - m) / T)", "std::exp(z[y] - m)"),
+    "philox key bump dropped": ("k[1] += PhiloxConst<W>::W1;", ""),
+    "philox words swapped": ("c[1] = lo1;", "c[1] = lo0;"),
+    "fanout exponent": ("(double)k / (1.0 + r)", "(double)k / r"),
+}
+
+PINS = [
+    P.test_philox_round_structure_matches_numpy_philox4x64,
+    P.test_softmax_matches_scipy_and_temperature,
+    P.test_top_n_matches_stable_library_sort,
+    lambda orc: [P.test_saguaro_closed_forms(orc, C) for C in (0.5, 0.3)],
+    P.test_accept_prob_rule,
+    P.test_residual_mass_is_total_variation,
+    P.test_inverse_cdf_matches_library_search,
+    lambda orc: P.test_losslessness_exact_enumeration(orc, 5, 3, 0.5, 1.0),
+    P.test_fanout_is_the_lagrange_optimum,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_detect_planted_mistake(orc, tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = orc.source_text()
+    assert src.count(old) == 1, name
+    path = orc.build_variant(src.replace(old, new), os.path.join(str(tmp_path), "mut.so"))
+    failed = []
+    with orc.use_library(path):
+        for pin in PINS:
+            try:
+                pin(orc)
+            except AssertionError:
+                failed.append(getattr(pin, "__name__", "lambda"))
+    assert failed, f"no pin caught: {name}"
