@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verification round on GB300.
+
+One step = one SSD verification round over one batch of synthetic logits
+already resident in HBM:
+  ssd_verify (online-softmax normalisers, fused top-F bonus guesses,
+  Saguaro-biased q', accept test, residual bonus draw)
+  -> ssd_cache_build_guesses (outcome cache from the guesses)
+  -> ssd_cache_lookup (hit / all-rows-hit of the verified outcomes).
+
+Default workload: large-batch stress, B=256, K=8, V=151936, fp32 logits,
+Zipf(1.05) head, draft = target + N(0, 1.2^2), T=1, fan-out budget 24
+(F = 5,4,4,3,2,2,2,1,1), C=0.5, cache of 256 x 24 keys.  The logits
+(2.80 GB) are larger than L2 (no flush needed).
+
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload on the host cores.  Under torchrun each rank runs its own batch
+(weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/sec and logits GB/s (fraction of GB300 HBM peak) at V=128k-152k"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def csrc_hash():
+    d = os.path.join(ROOT, "sampling_ssd_verify_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(workload):
+    """Per-launch DRAM bytes recorded by an ncu capture, if the kernels have
+    not changed since (profiles/<...>.md carries 'csrc_sha: <hash>' and
+    'traffic_bytes_per_launch[<workload>]: <n>')."""
+    pd = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pd):
+        return None
+    want = csrc_hash()
+    for f in sorted(os.listdir(pd)):
+        if not f.endswith(".md"):
+            continue
+        txt = open(os.path.join(pd, f)).read()
+        if f"csrc_sha: {want}" not in txt:
+            continue
+        key = f"traffic_bytes_per_launch[{workload}]:"
+        for line in txt.splitlines():
+            if line.strip().startswith(key):
+                return float(line.split(":", 1)[1].strip())
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------------------ ours
+def run_ours(args):
+    import torch
+    import torch.distributed as tdist
+
+    import sampling_ssd_verify_gb300 as ssd
+    from ssd_inputs import WORKLOADS, make_batch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssd.build()
+    w = WORKLOADS[args.workload]
+    B, K, Kq, V = w.B, w.K, w.Kq, w.V
+    F = np.asarray(w.fanout, dtype=np.int32)
+    bt = make_batch(w, seed=w.seed + 7919 * rank)
+    if w.dtype == "bf16":
+        tg = torch.from_numpy(bt["target"].view(np.int16)).to(dev).view(torch.bfloat16)
+        dg = torch.from_numpy(bt["draft"].view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        tg = torch.from_numpy(bt["target"]).to(dev)
+        dg = torch.from_numpy(bt["draft"]).to(dev)
+    seeds = torch.from_numpy(bt["seeds"].view(np.int64)).to(dev)
+    # drafts x_j ~ q'_j from the library's Saguaro sampler (one call per position)
+    tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    for j in range(K):
+        tok[:, j] = ssd.saguaro_sample(dg[:, j, :], w.T, w.C, int(F[j]), seeds, j, 0,
+                                       guesses=False, qprime=False)["token"]
+    tok = tok.contiguous()
+    ws = torch.empty(ssd.lib().ssd_verify_workspace_size(B, K, Kq, V), dtype=torch.uint8,
+                     device=dev)
+    out = {}
+    ssd.verify(tg, dg, tok, seeds, 0, F, w.C, w.T, workspace=ws, out=out)
+    table = torch.empty(ssd.cache_bytes(B * Kq * out["guesses"].shape[2]), dtype=torch.uint8,
+                        device=dev)
+    look = {"branch": torch.empty(B, dtype=torch.int32, device=dev),
+            "all_hit": torch.empty(1, dtype=torch.int32, device=dev)}
+    stream = torch.cuda.current_stream()
+    ev_v = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+
+    def step(r, evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        ssd.verify(tg, dg, tok, seeds, r, F, w.C, w.T, workspace=ws, out=out)
+        if evs is not None:
+            evs[1].record(stream)
+        ssd.cache_build_guesses(out["guesses"], table=table)
+        ssd.cache_lookup(table, out["accept_len"], out["bonus"], out=look)
+
+    for s in range(args.warmup):
+        step(1 + s)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    t0.record(stream)
+    for s in range(args.steps):
+        step(1000 + s, ev_v[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        tdist.barrier()
+    ck = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+    verify_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_v]))
+    alg = w.algorithmic_bytes()
+    hbm_peak, peak_kind = peaks()
+    achieved = alg / (verify_ms * 1e-3) / 1e9
+
+    # round statistics (untimed): acceptance, cache hit rate, all-rows-hit fraction
+    acc_sum, hits, all_hits, nr = 0.0, 0, 0, 100
+    for r in range(nr):
+        step(50_000 + r)
+        acc_sum += float(out["accept_len"].float().mean().item())
+        hits += int((look["branch"] >= 0).sum().item())
+        all_hits += int(look["all_hit"].item())
+    h = hits / (nr * B)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        ht = torch.from_numpy(bt["target"].view(np.int16) if w.dtype == "bf16" else bt["target"])
+        hd = torch.from_numpy(bt["draft"].view(np.int16) if w.dtype == "bf16" else bt["draft"])
+        ht, hd = ht.pin_memory(), hd.pin_memory()
+        htok = tok.cpu().pin_memory()
+        hseed = seeds.cpu().pin_memory()
+        res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                    for k, v in (("accept_len", out["accept_len"]), ("bonus", out["bonus"]),
+                                 ("branch", look["branch"]), ("all_hit", look["all_hit"]))}
+        tg_raw = tg.view(torch.int16) if w.dtype == "bf16" else tg
+        dg_raw = dg.view(torch.int16) if w.dtype == "bf16" else dg
+        ne = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step(r):
+            tg_raw.copy_(ht, non_blocking=True)
+            dg_raw.copy_(hd, non_blocking=True)
+            tok.copy_(htok, non_blocking=True)
+            seeds.copy_(hseed, non_blocking=True)
+            step(r)
+            res_host["accept_len"].copy_(out["accept_len"], non_blocking=True)
+            res_host["bonus"].copy_(out["bonus"], non_blocking=True)
+            res_host["branch"].copy_(look["branch"], non_blocking=True)
+            res_host["all_hit"].copy_(look["all_hit"], non_blocking=True)
+            stream.synchronize()
+
+        e2e_step(0)
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        for s in range(ne):
+            e2e_step(90_000 + s)
+        e2e_s = time.perf_counter() - w0
+        if world > 1:
+            tt = torch.tensor([e2e_s], device=dev)
+            tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+            e2e_s = float(tt.item())
+        h2d = int(ht.numel() * ht.element_size() + hd.numel() * hd.element_size()
+                  + htok.numel() * 4 + hseed.numel() * 8)
+        d2h = int(sum(v.numel() * v.element_size() for v in res_host.values()))
+        e2e = {"value": B * world * ne / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": ne}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        traffic = traffic_from_profile(args.workload)
+        line = {
+            "metric": METRIC,
+            "value": B * world * args.steps / (ms * 1e-3),
+            "unit": "rows/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32" if w.dtype == "f32" else "bf16",
+            "data": "synthetic (seeded Zipf-head / Gumbel logits over a random vocab permutation; "
+                    "drafts drawn by the library's Saguaro sampler)",
+            "config": {"workload": w.name, "B": B, "K": K, "Kq": Kq, "V": V, "T": w.T,
+                       "C": w.C, "fanout": list(map(int, F)), "global_batch": B * world,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else
+                             "inputs smaller than L2",
+                       "positions_per_s": (K + 1) * B * world * args.steps / (ms * 1e-3),
+                       "logits_gb_per_s": alg * world * args.steps / (ms * 1e-3) / 1e9,
+                       "accept_mean": acc_sum / nr, "hit_rate": h,
+                       "all_hit_fraction": all_hits / nr, "h_pow_B": h ** B,
+                       "wall_s_timed": wall},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic,
+                         "kernel": "ssd_verify (streaming pass + bonus draw)",
+                         "algorithmic_bytes_per_launch": alg, "launch_ms": verify_ms,
+                         "peak_kind": peak_kind},
+            "e2e": e2e,
+            "gpu_launches": 5 * args.steps,
+            "clocks": ck,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        tdist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------ oracle
+def cpu_baseline(w, seconds, rows_per_call=None):
+    """The CPU oracle, as it stands, on a bounded sample of the workload's
+    rows (all host threads)."""
+    from oracle import oracle as orc
+    from ssd_inputs import make_batch
+
+    cores = os.cpu_count() or 1
+    n = rows_per_call or max(4, min(w.B, 2 * cores))
+    rows = np.arange(n)
+    bt = make_batch(w, rows=rows)
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=w.K, nthreads=cores)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], done, F, w.C, w.T,
+                   nthreads=cores, row_ids=rows)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 1000:
+            break
+    return {"value": n * done / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.B} rows x {done} calls ({el:.1f} s), fp64 oracle, "
+                      f"{cores} threads"}
+
+
+def run_reference(args):
+    from ssd_inputs import WORKLOADS
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    n = max(4, min(w.B, 2 * cores))
+    from oracle import oracle as orc
+    from ssd_inputs import make_batch
+
+    rows = np.arange(n)
+    bt = make_batch(w, rows=rows)
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=w.K, nthreads=cores)
+
+    def step(r):
+        orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], r, F, w.C, w.T, nthreads=cores,
+                   row_ids=rows)
+
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(1000 + s)
+    el = time.perf_counter() - t0
+    v = n * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "K": w.K, "V": w.V},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {w.B} rows per step"},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c5", choices=["c2", "c3", "c4", "c5"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = 3 if args.steps is None else args.steps
+        args.warmup = 1 if args.warmup is None else args.warmup
+        run_reference(args)
+        return
+    args.steps = 2000 if args.steps is None else args.steps
+    args.warmup = 20 if args.warmup is None else max(3, args.warmup)
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

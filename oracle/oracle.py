@@ -68,7 +68,7 @@ def _configure(L):
                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                              ctypes.c_double, _i32p, _u64p, ctypes.c_uint32, _i32p,
                              ctypes.c_double, ctypes.c_int, _i32p, _i32p, _dp, _i32p, _dp,
-                             _dp, _dp, ctypes.c_int]
+                             _dp, _dp, ctypes.c_int, _i32p]
     L.orc_verify.restype = ctypes.c_int
     L.orc_topf_bonus.argtypes = [_vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_double, _i32p,
@@ -76,7 +76,7 @@ def _configure(L):
     L.orc_saguaro_sample.argtypes = [_vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                      ctypes.c_int, _u64p, ctypes.c_int, ctypes.c_uint32,
-                                     _i32p, _dp, _i32p, _dp, ctypes.c_int]
+                                     _i32p, _dp, _i32p, _dp, ctypes.c_int, _i32p]
     L.orc_cache_lookup.argtypes = [_i32p, _i32p, _i32p, _i32p, ctypes.c_int, _i32p, _i32p,
                                    ctypes.c_int, _i32p, _i32p]
     L.orc_cache_lookup.restype = ctypes.c_int
@@ -212,7 +212,8 @@ def _dtype_code(arr):
     raise TypeError(arr.dtype)
 
 
-def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1):
+def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1,
+           row_ids=None):
     """target [B,K+1,V], draft [B,Kq,V] (uint16 bf16 bits or float32)."""
     target = np.ascontiguousarray(target)
     draft = np.ascontiguousarray(draft)
@@ -235,7 +236,7 @@ def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1)
                           Kq, V, float(T), _p(tokens, _i32p), _p(seeds, _u64p), int(round_),
                           _p(F, _i32p), float(C), Fmax, _p(acc, _i32p), _p(bon, _i32p),
                           _p(Z, _dp), _p(g, _i32p), _p(gq, _dp), _p(ma, _dp), _p(mc, _dp),
-                          int(nthreads))
+                          int(nthreads), _p(None if row_ids is None else _i32(row_ids), _i32p))
     if rc:
         raise ValueError("draft token outside [0, V)")
     return dict(accept_len=acc, bonus=bon, resid_mass=Z, guesses=g, guess_q=gq,
@@ -256,7 +257,7 @@ def topf_bonus(draft, F, T, tokens=None, K=0, Fmax=None, nthreads=1):
     return dict(guesses=g, guess_q=gq)
 
 
-def saguaro_sample(rows, T, C, F, seeds, j, round_, nthreads=1):
+def saguaro_sample(rows, T, C, F, seeds, j, round_, nthreads=1, row_ids=None):
     """rows [R, V] (uint16 bf16 bits or float32)."""
     rows = np.ascontiguousarray(rows)
     R, V = rows.shape
@@ -267,7 +268,8 @@ def saguaro_sample(rows, T, C, F, seeds, j, round_, nthreads=1):
     mc = np.zeros(R)
     lib().orc_saguaro_sample(rows.ctypes.data, _dtype_code(rows), V, R, V, float(T), float(C),
                              int(F), _p(seeds, _u64p), int(j), int(round_), _p(tok, _i32p),
-                             _p(qp, _dp), _p(g, _i32p), _p(mc, _dp), int(nthreads))
+                             _p(qp, _dp), _p(g, _i32p), _p(mc, _dp), int(nthreads),
+                             _p(None if row_ids is None else _i32(row_ids), _i32p))
     return dict(token=tok, qprime=qp, guesses=g[:, :F], margin_cdf=mc)
 
 

@@ -293,13 +293,15 @@ int orc_inverse_cdf(const double* w, int V, double Z, double u, double* margin) 
 //   guesses_j = top-(F_j+1) of z_q[j] minus x_j (j < K), truncated to F_j.
 // Reading: verification uses q', the distribution the drafts were drawn from
 // ([SSD-note] §"解法：操纵草稿分布": lowering q on cached tokens raises (p-q)^+).
+// row_ids (or NULL = 0..B-1) give each row's Philox counter word 0, so a
+// sample of rows of a larger batch can be checked one by one.
 // Returns 0, or 1 if a draft token lies outside [0, V).
 int orc_verify(const void* target, const void* draft, int dtype, int64_t t_stride,
                int64_t d_stride, int B, int K, int Kq, int V, double T,
                const int32_t* tokens, const uint64_t* seeds, uint32_t round,
                const int32_t* F, double C, int Fmax, int32_t* accept_len, int32_t* bonus,
                double* resid_mass, int32_t* guesses, double* guess_q, double* margin_accept,
-               double* margin_cdf, int nthreads) {
+               double* margin_cdf, int nthreads, const int32_t* row_ids) {
   for (int i = 0; i < B * K; ++i)
     if (tokens[i] < 0 || tokens[i] >= V) return 1;
   parallel_rows(B, nthreads, [&](int b) {
@@ -311,6 +313,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
       top1[j] = top_n(zq[j], F[j] + 1);
     }
     const int32_t* x = tokens + (int64_t)b * K;
+    const uint32_t rid = row_ids ? (uint32_t)row_ids[b] : (uint32_t)b;  // Philox counter word 0
     int k = K;
     double mA = INFINITY;
     std::vector<double> p_k;
@@ -321,7 +324,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
       std::vector<int> S(top1[i].begin(), top1[i].begin() + std::min<int>(F[i], top1[i].size()));
       auto qp = saguaro(q[i], S, C);
       double r = p[x[i]] / qp[x[i]];
-      double u = uniform24(seeds[b], (uint32_t)b, (uint32_t)i, 0u, round);
+      double u = uniform24(seeds[b], rid, (uint32_t)i, 0u, round);
       mA = std::min(mA, std::fabs(u - r));
       if (!(u < r)) {
         k = i;
@@ -341,7 +344,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
       for (double v : w) Z += v;
     }
     double mC = 0.0;
-    double u2 = uniform24(seeds[b], (uint32_t)b, (uint32_t)k, 1u, round);
+    double u2 = uniform24(seeds[b], rid, (uint32_t)k, 1u, round);
     int t;
     if (Z > 1e-30) {
       t = inverse_cdf(w, Z, u2, &mC);
@@ -402,7 +405,7 @@ int orc_topf_bonus(const void* draft, int dtype, int64_t d_stride, int B, int Kq
 int orc_saguaro_sample(const void* draft, int dtype, int64_t stride, int R, int V, double T,
                        double C, int F, const uint64_t* seeds, int j, uint32_t round,
                        int32_t* out_token, double* out_qprime, int32_t* out_guess,
-                       double* margin_cdf, int nthreads) {
+                       double* margin_cdf, int nthreads, const int32_t* row_ids) {
   parallel_rows(R, nthreads, [&](int r) {
     auto z = load_row(draft, dtype, (int64_t)r * stride, V);
     auto q = softmax(z, T);
@@ -411,7 +414,8 @@ int orc_saguaro_sample(const void* draft, int dtype, int64_t stride, int R, int 
     auto qp = saguaro(q, S, C);
     double Z = 0.0;
     for (double v : qp) Z += v;
-    double u = uniform24(seeds[r], (uint32_t)r, (uint32_t)j, 2u, round);
+    const uint32_t rid = row_ids ? (uint32_t)row_ids[r] : (uint32_t)r;
+    double u = uniform24(seeds[r], rid, (uint32_t)j, 2u, round);
     double m = 0.0;
     int x = inverse_cdf(qp, Z, u, &m);
     out_token[r] = x;

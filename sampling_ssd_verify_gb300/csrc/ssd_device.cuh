@@ -1,0 +1,354 @@
+// ssd_device.cuh -- device helpers: inline-PTX wrappers for mbarriers and
+// bulk copies, bounded waits, Philox-4x32-10, exponent and reduction helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+// ---- shared-memory addressing, mbarriers, bulk copies ---------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, for at most
+// kWaitLimitNs.  On time-out the error flag is raised (shared flag and the
+// caller's device status) and false is returned; the caller then carries on
+// without the data so that every thread still reaches every barrier.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* s_err,
+                                          int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (*s_err) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *s_err = 1;
+      if (status) atomicOr(status, SSD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Named barrier over the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// ---- optional bounds checks (compile with -DSSD_CHECKS) ---------------------------
+// A failed check records (code, a, b, block, thread) once in the workspace's
+// debug record, counts the failure and skips the guarded access.
+#ifdef SSD_CHECKS
+__device__ __forceinline__ bool ssd_chk(bool ok, unsigned long long* dbg, int code, long long a,
+                                        long long b) {
+  if (ok) return true;
+  if (dbg != nullptr) {
+    if (atomicCAS(dbg, 0ull, (unsigned long long)code) == 0ull) {
+      dbg[1] = (unsigned long long)a;
+      dbg[2] = (unsigned long long)b;
+      dbg[3] = blockIdx.x;
+      dbg[4] = threadIdx.x;
+    }
+    atomicAdd(dbg + 5, 1ull);
+  }
+  return false;
+}
+#define SSD_CHK(ok, dbg, code, a, b) ::ssd::ssd_chk((ok), (dbg), (code), (long long)(a), (long long)(b))
+#else
+#define SSD_CHK(ok, dbg, code, a, b) true
+#endif
+
+__device__ __forceinline__ bool in_range(uintptr_t a0, uintptr_t a1, const char* lo,
+                                         const char* hi) {
+  return a0 >= (uintptr_t)lo && a1 <= (uintptr_t)hi && a0 <= a1;
+}
+
+// ---- element access ---------------------------------------------------------------
+template <int DT>
+struct Elem;
+template <>
+struct Elem<0> {  // bf16
+  static constexpr int kSize = 2;
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float load(const void* base, int64_t i) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + i);
+    return __uint_as_float(((uint32_t)h) << 16);
+  }
+  __device__ __forceinline__ static float load_cg(const void* base, int64_t i) {
+    const unsigned short h = __ldcg(reinterpret_cast<const unsigned short*>(base) + i);
+    return __uint_as_float(((uint32_t)h) << 16);
+  }
+  __device__ __forceinline__ static float smem(const void* base, int i) {
+    const unsigned short h = reinterpret_cast<const unsigned short*>(base)[i];
+    return __uint_as_float(((uint32_t)h) << 16);
+  }
+  __device__ __forceinline__ static void unpack(const uint4 v, float* x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(w[k] << 16);
+      x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+};
+template <>
+struct Elem<1> {  // fp32
+  static constexpr int kSize = 4;
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static float load(const void* base, int64_t i) {
+    return __ldg(reinterpret_cast<const float*>(base) + i);
+  }
+  __device__ __forceinline__ static float load_cg(const void* base, int64_t i) {
+    return __ldcg(reinterpret_cast<const float*>(base) + i);
+  }
+  __device__ __forceinline__ static float smem(const void* base, int i) {
+    return reinterpret_cast<const float*>(base)[i];
+  }
+  __device__ __forceinline__ static void unpack(const uint4 v, float* x) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  }
+};
+
+__device__ __forceinline__ const char* row_ptr(const void* base, int64_t row, int64_t stride,
+                                               int esize) {
+  return reinterpret_cast<const char*>(base) + row * stride * esize;
+}
+
+// ---- arithmetic helpers -------------------------------------------------------------
+// 2^x with the SFU (ex2.approx.ftz.f32).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Error-free sum of two floats (Knuth): a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// Compensated pair addition (hi, lo) += (bhi, blo).
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float bhi, float blo) {
+  float s, e;
+  two_sum(hi, bhi, s, e);
+  e += lo + blo;
+  hi = s + e;
+  lo = e - (hi - s);
+}
+
+// Scale a compensated pair by f (keeps the product's rounding error).
+__device__ __forceinline__ void pair_scale(float& hi, float& lo, float f) {
+  const float p = hi * f;
+  const float perr = fmaf(hi, f, -p);
+  lo = fmaf(lo, f, perr);
+  hi = p;
+}
+
+// ---- Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) ---------------------------------
+// Round: (c0, c1, c2, c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)),
+// key += (0x9E3779B9, 0xBB67AE85) between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// u = (out0 >> 8) * 2^-24 for key = seed, counter = (c0, c1, stream, round).
+__device__ __forceinline__ double uniform24(uint64_t seed, uint32_t c0, uint32_t c1,
+                                            uint32_t stream, uint32_t round) {
+  const uint4 o = philox4x32_10(make_uint4(c0, c1, stream, round),
+                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  return (double)(o.x >> 8) * (1.0 / 16777216.0);
+}
+
+// ---- candidate lists (top-F by raw logit, ties to the lower index) -----------------------
+__device__ __forceinline__ bool cand_before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// Insert (x, ix) into a descending list of TOPK entries.  Elements of one
+// thread arrive in increasing index order, so a strict comparison keeps the
+// lower index first among equal logits.
+template <int TOPK>
+__device__ __forceinline__ void topk_insert(float (&tv)[TOPK > 0 ? TOPK : 1],
+                                            int (&ti)[TOPK > 0 ? TOPK : 1], float x, int ix) {
+#pragma unroll
+  for (int k = TOPK - 1; k >= 0; --k) {
+    const float up = (k > 0) ? tv[k > 0 ? k - 1 : 0] : __int_as_float(0x7f800000);
+    const int upi = (k > 0) ? ti[k > 0 ? k - 1 : 0] : 0;
+    if (x > tv[k]) {
+      if (x > up) {
+        tv[k] = up;
+        ti[k] = upi;
+      } else {
+        tv[k] = x;
+        ti[k] = ix;
+      }
+    }
+  }
+}
+
+// Insert with the full (value desc, index asc) order, for merges of lists
+// whose elements do not arrive in index order.
+template <int TOPK>
+__device__ __forceinline__ void topk_insert_ordered(float (&tv)[TOPK > 0 ? TOPK : 1],
+                                                    int (&ti)[TOPK > 0 ? TOPK : 1], float x,
+                                                    int ix) {
+#pragma unroll
+  for (int k = TOPK - 1; k >= 0; --k) {
+    const bool above_k = cand_before(x, ix, tv[k], ti[k]);
+    const bool above_up = (k == 0) ? false : cand_before(x, ix, tv[k > 0 ? k - 1 : 0],
+                                                         ti[k > 0 ? k - 1 : 0]);
+    if (above_k) {
+      if (above_up) {
+        tv[k] = tv[k > 0 ? k - 1 : 0];
+        ti[k] = ti[k > 0 ? k - 1 : 0];
+      } else {
+        tv[k] = x;
+        ti[k] = ix;
+      }
+    }
+  }
+}
+
+// Merge the per-lane descending lists of a warp into one list of TOPK,
+// returned identically in every lane (iterative extraction of the warp
+// maximum under a strict total order: value desc, index asc, lane asc).
+template <int TOPK>
+__device__ __forceinline__ void warp_topk_merge(float (&tv)[TOPK > 0 ? TOPK : 1],
+                                                int (&ti)[TOPK > 0 ? TOPK : 1]) {
+  const int lane = threadIdx.x & 31;
+  float ov[TOPK > 0 ? TOPK : 1];
+  int oi[TOPK > 0 ? TOPK : 1];
+#pragma unroll
+  for (int r = 0; r < TOPK; ++r) {
+    float bv = tv[0];
+    int bi = ti[0];
+    int bl = lane;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+      const int l2 = __shfl_xor_sync(0xffffffffu, bl, off);
+      const bool take = v2 > bv || (v2 == bv && (i2 < bi || (i2 == bi && l2 < bl)));
+      if (take) {
+        bv = v2;
+        bi = i2;
+        bl = l2;
+      }
+    }
+    ov[r] = bv;
+    oi[r] = bi;
+    if (lane == bl) {  // pop the head of the winning lane's list
+#pragma unroll
+      for (int k = 0; k < TOPK - 1; ++k) {
+        tv[k] = tv[k + 1];
+        ti[k] = ti[k + 1];
+      }
+      tv[TOPK - 1] = __int_as_float(0xff800000);
+      ti[TOPK - 1] = 0x7fffffff;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < TOPK; ++r) {
+    tv[r] = ov[r];
+    ti[r] = oi[r];
+  }
+}
+
+// Warp-wide merge of (max, compensated sum) partials.  Each lane holds
+// (m, mc = fl(m*c), hi, lo) with the sum taken relative to mc; returns the
+// warp maximum M and the sum relative to fl(M*c) in every lane.
+__device__ __forceinline__ void warp_softmax_merge(float m, float mc, float hi, float lo, float c,
+                                                   float& M, float& MC, float& Shi,
+                                                   float& Slo) {
+  M = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  MC = __fmul_rn(M, c);
+  float h = hi, l = lo;
+  if (m == __int_as_float(0xff800000)) {
+    h = 0.f;
+    l = 0.f;
+  } else if (mc != MC) {
+    pair_scale(h, l, exp2f(mc - MC));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, h, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    pair_add(h, l, h2, l2);
+  }
+  Shi = h;
+  Slo = l;
+}
+
+}  // namespace ssd

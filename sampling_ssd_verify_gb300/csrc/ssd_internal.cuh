@@ -1,0 +1,180 @@
+// ssd_internal.cuh -- shared definitions of the CUDA library (not part of
+// the public ABI): tuning constants, kernel parameter blocks, workspace
+// records and small device helpers (PTX wrappers, Philox, reductions).
+//
+// Sources, cited by page title and section:
+//   [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈"
+//   [SD-7.3]   "7.3 Speculative Decoding：投机采样加速"
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// ---- tuning ------------------------------------------------------------------
+constexpr int kConsumerWarps = 8;                   // warps that reduce staged data
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;           // + one producer (bulk-copy) warp
+constexpr int kUnitA = 1024;                        // elements per work unit, streaming pass
+constexpr int kStageBytes = 16384;                  // bytes per pipeline stage
+constexpr int kStagesA = 8;                         // ring depth, streaming pass
+constexpr int kUnitB = 512;                         // elements per unit, CDF pass
+constexpr int kUnitsPerStageB = kConsumerWarps;     // one unit per consumer warp
+constexpr int kStagesB = 4;                         // ring depth, CDF pass
+constexpr int kMaxTopK = 16;                        // per-row candidate list (F + 1 <= 16)
+constexpr int kMaxGrid = 4096;                      // bound on CTAs of one launch
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
+
+enum Mode : int { kModeVerify = 0, kModeTopF = 1, kModeSaguaro = 2 };
+
+// Per-(CTA, row piece) partial of the streaming pass.
+struct RowPartial {
+  float m;        // max raw logit of the piece
+  float pad;
+  float s_hi;     // sum of exp2(z*c - fl(m*c)) as a compensated pair
+  float s_lo;
+  float tv[kMaxTopK];
+  int ti[kMaxTopK];
+};
+
+// Final per-row statistics.
+struct RowResult {
+  float m;        // max raw logit
+  float mc;       // fl32(m * c): the offset every exponent of the row used
+  double s;       // sum_y exp2(fl(z_y*c - mc))
+  float zx;       // logit of the row's draft token (if the row has one)
+  int x;
+  float tv[kMaxTopK];  // top raw logits, descending, ties to the lower index
+  int ti[kMaxTopK];
+};
+
+// Per-group (sequence / branch row) parameters of the CDF pass, written by
+// the group epilogue of the streaming pass.
+struct GroupParams {
+  int k;            // verify: accept length; rows read by the CDF pass: see below
+  int use_t;        // the CDF weight has a target term p(y)
+  int use_d;        // the CDF weight has a draft term q'(y)
+  int sign_d;       // +1: w = q'(y) (Saguaro draw), -1: w = (p(y) - q'(y))^+
+  int64_t row_t;    // target row index (into the target tensor)
+  int64_t row_d;    // draft row index (into the draft tensor)
+  float mc_t, inv_st;        // p(y) = exp2(fl(z*c - mc_t)) * inv_st
+  float mc_d, scale_out, scale_in;  // q'(y) = exp2(fl(z*c - mc_d)) * (in S ? scale_in : scale_out)
+  float theta;      // S = { y : z > theta or (z == theta and y <= itheta) }
+  int itheta;
+  double u;         // uniform of the draw
+};
+
+struct StreamParams {
+  const void* tgt;
+  int64_t t_stride;
+  const void* dft;
+  int64_t d_stride;
+  int B, K, Kq, V;
+  int nt, nd, rpg;          // target rows, draft rows per group, rows per group
+  int64_t NR;               // rows in total
+  int upr;                  // units per row
+  int64_t total_units;
+  int64_t upc;              // units per CTA
+  float c;                  // log2(e) / T
+  float C;
+  int F[SSD_MAX_K + 1];
+  int need_top;             // draft rows keep a top list
+  const int32_t* tokens;    // [groups, tokK] or null
+  int tokK;
+  const uint64_t* seeds;
+  uint32_t round;
+  int jpos;                 // Saguaro: continuation position
+  int mode;
+  int32_t* accept_len;
+  int32_t* guesses;         // [groups, nd, Fmax]
+  float* guess_q;
+  int Fmax;
+  int* row_cnt;
+  int* grp_cnt;
+  RowPartial* partials;     // slot (row + cta)
+  RowResult* rowres;
+  GroupParams* gparams;
+  int32_t* status;
+  // bounds of the inputs and the debug record (used by SSD_CHECKS builds)
+  const char* t_lo;
+  const char* t_hi;
+  const char* d_lo;
+  const char* d_hi;
+  unsigned long long* dbg;
+};
+
+struct CdfParams {
+  const void* tgt;
+  int64_t t_stride;
+  const void* dft;
+  int64_t d_stride;
+  int groups, V, nsub;
+  int64_t total_units;
+  int64_t upc;
+  float c;
+  int mode;
+  const GroupParams* gp;
+  const RowResult* rowres;  // Saguaro: the branch row's top list
+  int rpg, nt;
+  float* subsum;            // [groups, nsub]
+  int* cnt;                 // [groups]
+  int32_t* out_token;
+  float* out_mass;          // verify: resid mass
+  float* out_qprime;        // Saguaro: q'(x)
+  int32_t* out_guess;       // Saguaro: [groups, F]
+  int F;
+  int32_t* status;
+  const char* t_lo;
+  const char* t_hi;
+  const char* d_lo;
+  const char* d_hi;
+  unsigned long long* dbg;
+};
+
+// ---- workspace layout ----------------------------------------------------------
+struct WsLayout {
+  size_t cnt_off, cnt_bytes;       // counters (cleared each call)
+  size_t part_off, rowres_off, gp_off, sub_off, dbg_off, total;
+  int64_t NR;
+  int groups, nsub;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline WsLayout ws_layout(int groups, int rpg, int V) {
+  WsLayout L;
+  L.groups = groups;
+  L.NR = (int64_t)groups * rpg;
+  L.nsub = (V + kUnitB - 1) / kUnitB;
+  size_t ncnt = (size_t)L.NR + 2 * (size_t)groups;
+  L.cnt_off = 0;
+  L.cnt_bytes = align256(ncnt * sizeof(int));
+  L.part_off = L.cnt_bytes;
+  L.rowres_off = L.part_off + align256(((size_t)L.NR + kMaxGrid) * sizeof(RowPartial));
+  L.gp_off = L.rowres_off + align256((size_t)L.NR * sizeof(RowResult));
+  L.sub_off = L.gp_off + align256((size_t)groups * sizeof(GroupParams));
+  L.dbg_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));
+  L.total = L.dbg_off + 256;  // bounds-check record of SSD_CHECKS builds
+  return L;
+}
+
+// ---- launchers (defined in ssd_stream.cu / ssd_cdf.cu / ssd_cache.cu) -----------
+cudaError_t launch_stream(const StreamParams& p, int dtype, int topk, int grid,
+                          cudaStream_t s);
+cudaError_t launch_cdf(const CdfParams& p, int dtype, int grid, cudaStream_t s);
+cudaError_t launch_cache_clear(void* table, int64_t capacity, cudaStream_t s);
+cudaError_t launch_cache_insert(void* table, int64_t capacity, const int32_t* row,
+                                const int32_t* k, const int32_t* t, const int32_t* branch, int n,
+                                const int32_t* guesses, int B, int Kq, int Fmax,
+                                int32_t* status, cudaStream_t s);
+cudaError_t launch_cache_lookup(const void* table, int64_t capacity, const int32_t* accept_len,
+                                const int32_t* bonus, int B, int32_t* out_branch,
+                                int32_t* all_hit, cudaStream_t s);
+int stream_smem_bytes();
+int cdf_smem_bytes(int dtype);
+int num_sms();
+
+}  // namespace ssd

@@ -1,0 +1,594 @@
+// ssd_stream.cu -- the streaming pass over full-vocabulary logit rows.
+//
+// One persistent CTA per SM takes an equal, contiguous share of the
+// flattened (row, 1024-element unit) space.  A producer warp streams the
+// share through a ring of 16 KB shared-memory stages with 1-D bulk copies
+// (cp.async.bulk + mbarrier transaction counts); eight consumer warps reduce
+// each row piece to
+//   * the online-softmax normaliser: max raw logit m and
+//     s = sum_y 2^(z_y * c - fl(m*c)), c = log2(e)/T, accumulated with
+//     per-thread compensated sums ([SD-7.3] §7.3.2: the target and draft
+//     distributions at every position);
+//   * for draft rows, the top-(F_j+1) raw logits (ties to the lower index):
+//     the bonus-token guesses and the Saguaro cached set
+//     ([SSD-note] §"怎么猜奖励 token", §"Saguaro 优化二：Saguaro 采样").
+// Rows split across CTAs are merged by the last CTA to finish them (atomic
+// arrival counter); the last row of a sequence to be finalised runs the
+// sequence epilogue: the warp-parallel accept test min(1, p/q') with the
+// first-rejection scan ([SD-7.3] §7.3.3; [SD-blog] §"三、接受概率为什么是对的"),
+// or, for Saguaro sampling, the parameters of the continuation draw.
+//
+// Sources: [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈";
+// [SD-7.3] "7.3 Speculative Decoding：投机采样加速";
+// [SD-blog] "推测解码：用一个“小模型”骗出 3 倍推理速度".
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd_device.cuh"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr float kNegInf = -INFINITY;
+constexpr float kPosInf = INFINITY;
+
+template <int TOPK>
+struct alignas(16) PieceRed {
+  float m[kConsumerWarps];
+  float hi[kConsumerWarps];
+  float lo[kConsumerWarps];
+  float tv[kConsumerWarps][TOPK > 0 ? TOPK : 1];
+  int ti[kConsumerWarps][TOPK > 0 ? TOPK : 1];
+};
+
+// Geometry of one pipeline stage: the element range [e0, e1) of row `row`
+// and its 16-byte-aligned interior [a0, a1) (byte addresses).
+struct Stage {
+  int64_t row;
+  int e0, e1;
+  uintptr_t b0, a0, a1;
+};
+
+template <int DT>
+__device__ __forceinline__ const void* tensor_of(const StreamParams& p, int64_t row,
+                                                 int64_t& trow, bool& is_t) {
+  const int64_t g = row / p.rpg;
+  const int jr = (int)(row - g * p.rpg);
+  is_t = jr < p.nt;
+  if (is_t) {
+    trow = g * (p.K + 1) + jr;
+    return p.tgt;
+  }
+  trow = g * p.Kq + (jr - p.nt);
+  return p.dft;
+}
+
+template <int DT>
+__device__ __forceinline__ Stage stage_geometry(const StreamParams& p, int64_t row, int64_t u,
+                                                int64_t un) {
+  Stage st;
+  st.row = row;
+  const int64_t ur = row * p.upr;
+  st.e0 = (int)((u - ur) * kUnitA);
+  st.e1 = (int)min((int64_t)p.V, (un - ur) * kUnitA);
+  int64_t trow;
+  bool is_t;
+  const void* base = tensor_of<DT>(p, row, trow, is_t);
+  const int64_t stride = is_t ? p.t_stride : p.d_stride;
+  const char* rp = row_ptr(base, trow, stride, Elem<DT>::kSize);
+  st.b0 = (uintptr_t)(rp + (int64_t)st.e0 * Elem<DT>::kSize);
+  const uintptr_t b1 = (uintptr_t)(rp + (int64_t)st.e1 * Elem<DT>::kSize);
+  st.a0 = (st.b0 + 15) & ~(uintptr_t)15;
+  st.a1 = b1 & ~(uintptr_t)15;
+  if (st.a1 <= st.a0) st.a0 = st.a1 = st.b0;  // no aligned interior: all scalar
+  return st;
+}
+
+// Per-thread accumulator of one row piece.
+template <int TOPK>
+struct Acc {
+  float m, mc, hi, lo;
+  float tv[TOPK > 0 ? TOPK : 1];
+  int ti[TOPK > 0 ? TOPK : 1];
+  __device__ __forceinline__ void reset() {
+    m = kNegInf;
+    mc = kNegInf;
+    hi = 0.f;
+    lo = 0.f;
+#pragma unroll
+    for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
+      tv[k] = kNegInf;
+      ti[k] = 0x7fffffff;
+    }
+  }
+  // Raise the running maximum to vm (rescaling the sum).
+  __device__ __forceinline__ void raise_max(float vm, float c) {
+    const float mcn = __fmul_rn(vm, c);
+    if (m != kNegInf) pair_scale(hi, lo, exp2f(mc - mcn));
+    m = vm;
+    mc = mcn;
+  }
+  // Kahan-style compensated accumulation of a (positive) partial sum.
+  __device__ __forceinline__ void add(float v) {
+    const float y = v - lo;
+    const float t = hi + y;
+    lo = (t - hi) - y;
+    hi = t;
+  }
+};
+
+template <int DT, int TOPK>
+__device__ __forceinline__ void consume_vec(Acc<TOPK>& a, const uint4 raw, int idx0, float c,
+                                            bool top) {
+  constexpr int VEC = Elem<DT>::kVec;
+  float x[VEC];
+  Elem<DT>::unpack(raw, x);
+  float vm = x[0];
+#pragma unroll
+  for (int k = 1; k < VEC; ++k) vm = fmaxf(vm, x[k]);
+  if (vm > a.m) a.raise_max(vm, c);
+  float e[VEC];
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(x[k], c, -a.mc));
+#pragma unroll
+  for (int w = VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) e[k] += e[k + w];
+  a.add(e[0]);
+  if constexpr (TOPK > 0) {
+    if (top && vm > a.tv[TOPK - 1]) {
+#pragma unroll
+      for (int k = 0; k < VEC; ++k)
+        if (x[k] > a.tv[TOPK - 1]) topk_insert<TOPK>(a.tv, a.ti, x[k], idx0 + k);
+    }
+  }
+}
+
+// Unaligned head/tail elements of a stage.  Head elements precede the stage's
+// vectors in vocabulary order but are folded in after them, so candidates are
+// inserted with the full (logit desc, index asc) order.
+template <int TOPK>
+__device__ __forceinline__ void consume_one(Acc<TOPK>& a, float x, int idx, float c, bool top) {
+  if (x > a.m) a.raise_max(x, c);
+  a.add(ex2(fmaf(x, c, -a.mc)));
+  if constexpr (TOPK > 0) {
+    if (top && cand_before(x, idx, a.tv[TOPK - 1], a.ti[TOPK - 1]))
+      topk_insert_ordered<TOPK>(a.tv, a.ti, x, idx);
+  }
+}
+
+// Fold one stored partial into a lane's accumulator (row merges).
+template <int TOPK>
+__device__ __forceinline__ void fold_partial(Acc<TOPK>& a, const RowPartial* pp, float c,
+                                             bool top) {
+  const float m2 = __ldcg(&pp->m);
+  const float h2 = __ldcg(&pp->s_hi);
+  const float l2 = __ldcg(&pp->s_lo);
+  if (m2 != kNegInf) {
+    float hh = h2, ll = l2;
+    const float mc2 = __fmul_rn(m2, c);
+    if (m2 > a.m) {
+      a.raise_max(m2, c);
+    } else if (mc2 != a.mc) {
+      pair_scale(hh, ll, exp2f(mc2 - a.mc));
+    }
+    pair_add(a.hi, a.lo, hh, ll);
+  }
+  if constexpr (TOPK > 0) {
+    if (top) {
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) {
+        const float v = __ldcg(&pp->tv[k]);
+        const int i = __ldcg(&pp->ti[k]);
+        if (v != kNegInf) topk_insert_ordered<TOPK>(a.tv, a.ti, v, i);
+      }
+    }
+  }
+}
+
+// ---- the sequence epilogue of ssd_verify (warp 0 of the finishing CTA) -----------------
+__device__ void verify_epilogue(const StreamParams& p, int64_t g) {
+  const int lane = threadIdx.x & 31;
+  const int K = p.K;
+  const double c = (double)p.c;
+  bool acc = true;
+  if (lane < K) {
+    const RowResult* rt = p.rowres + g * p.rpg + lane;
+    const RowResult* rd = p.rowres + g * p.rpg + p.nt + lane;
+    const int x = __ldcg(&rt->x);
+    const double pt = exp2((double)__ldcg(&rt->zx) * c - (double)__ldcg(&rt->mc)) / __ldcg(&rt->s);
+    const double sq = __ldcg(&rd->s);
+    const double mcq = (double)__ldcg(&rd->mc);
+    double qp = exp2((double)__ldcg(&rd->zx) * c - mcq) / sq;
+    const int F = p.F[lane];
+    if (p.C < 1.f && F > 0) {
+      double QS = 0.0;
+      bool inS = false;
+      for (int f = 0; f < F; ++f) {
+        QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), p.c, -__ldcg(&rd->mc)));
+        inS |= __ldcg(&rd->ti[f]) == x;
+      }
+      QS /= sq;
+      qp = qp * (inS ? (double)p.C : 1.0) / (1.0 - (1.0 - (double)p.C) * QS);
+    }
+    const double r = pt / qp;
+    const double u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)lane, 0u, p.round);
+    acc = u < r;
+  }
+  const unsigned rej = ~__ballot_sync(0xffffffffu, acc) & (K >= 32 ? 0xffffffffu : ((1u << K) - 1u));
+  const int k = rej ? __ffs(rej) - 1 : K;
+  if (lane == 0) {
+    if (!SSD_CHK(g < p.B && k >= 0 && k <= K, p.dbg, 8, g, k)) return;
+    p.accept_len[g] = k;
+    GroupParams gp;
+    const RowResult* rt = p.rowres + g * p.rpg + k;
+    gp.k = k;
+    gp.use_t = 1;
+    gp.row_t = g * (int64_t)(K + 1) + k;
+    gp.mc_t = __ldcg(&rt->mc);
+    gp.inv_st = (float)(1.0 / __ldcg(&rt->s));
+    gp.sign_d = -1;
+    gp.theta = kPosInf;
+    gp.itheta = -1;
+    if (k < K) {
+      const RowResult* rd = p.rowres + g * p.rpg + p.nt + k;
+      gp.use_d = 1;
+      gp.row_d = g * (int64_t)p.Kq + k;
+      gp.mc_d = __ldcg(&rd->mc);
+      const double sq = __ldcg(&rd->s);
+      double scale_out = 1.0 / sq, scale_in = 1.0 / sq;
+      const int F = p.F[k];
+      if (p.C < 1.f && F > 0) {
+        double QS = 0.0;
+        for (int f = 0; f < F; ++f)
+          QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), p.c, -gp.mc_d));
+        QS /= sq;
+        const double gn = 1.0 / (1.0 - (1.0 - (double)p.C) * QS);
+        scale_out = gn / sq;
+        scale_in = gn * (double)p.C / sq;
+        gp.theta = __ldcg(&rd->tv[F - 1]);
+        gp.itheta = __ldcg(&rd->ti[F - 1]);
+      }
+      gp.scale_out = (float)scale_out;
+      gp.scale_in = (float)scale_in;
+    } else {
+      gp.use_d = 0;
+      gp.row_d = 0;
+      gp.mc_d = 0.f;
+      gp.scale_out = gp.scale_in = 0.f;
+    }
+    gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)k, 1u, p.round);
+    p.gparams[g] = gp;
+  }
+}
+
+// Saguaro continuation draw: parameters of q' for branch row g.
+__device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResult& rr) {
+  GroupParams gp;
+  gp.k = 0;
+  gp.use_t = 0;
+  gp.use_d = 1;
+  gp.sign_d = 1;
+  gp.row_t = 0;
+  gp.row_d = g;
+  gp.mc_t = 0.f;
+  gp.inv_st = 0.f;
+  gp.mc_d = rr.mc;
+  gp.theta = kPosInf;
+  gp.itheta = -1;
+  double scale_out = 1.0 / rr.s, scale_in = 1.0 / rr.s;
+  const int F = p.F[0];
+  if (p.C < 1.f && F > 0) {
+    double QS = 0.0;
+    for (int f = 0; f < F; ++f) QS += (double)exp2f(fmaf(rr.tv[f], p.c, -rr.mc));
+    QS /= rr.s;
+    const double gn = 1.0 / (1.0 - (1.0 - (double)p.C) * QS);
+    scale_out = gn / rr.s;
+    scale_in = gn * (double)p.C / rr.s;
+    gp.theta = rr.tv[F - 1];
+    gp.itheta = rr.ti[F - 1];
+  }
+  gp.scale_out = (float)scale_out;
+  gp.scale_in = (float)scale_in;
+  gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)p.jpos, 2u, p.round);
+  p.gparams[g] = gp;
+}
+
+// Finalise row `row` from the merged (M, MC, S, top list) held by warp 0.
+template <int DT, int TOPK>
+__device__ void finalize_row(const StreamParams& p, int64_t row, float M, float MC, float Shi,
+                             float Slo, const Acc<TOPK>& a, bool top) {
+  const int lane = threadIdx.x & 31;
+  const int64_t g = row / p.rpg;
+  const int jr = (int)(row - g * p.rpg);
+  const bool is_t = jr < p.nt;
+  const int j = is_t ? jr : jr - p.nt;
+  RowResult rr;
+  rr.m = M;
+  rr.mc = MC;
+  rr.s = (double)Shi + (double)Slo;
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    const bool valid = TOPK > 0 && top && k < TOPK && a.tv[k < TOPK ? k : 0] != kNegInf;
+    rr.tv[k] = valid ? a.tv[k < TOPK ? k : 0] : kNegInf;
+    rr.ti[k] = valid ? a.ti[k < TOPK ? k : 0] : -1;
+  }
+  rr.x = -1;
+  rr.zx = 0.f;
+  if (p.tokens != nullptr && j < p.tokK) {
+    int x = SSD_CHK(g < p.B && j < p.tokK, p.dbg, 3, g, j) ? p.tokens[g * p.tokK + j] : 0;
+    if (x < 0 || x >= p.V) {
+      if (lane == 0 && p.status) atomicOr(p.status, SSD_DEV_BAD_TOKEN);
+      x = 0;
+    }
+    int64_t trow;
+    bool it;
+    const void* base = tensor_of<DT>(p, row, trow, it);
+    const char* rp = row_ptr(base, trow, it ? p.t_stride : p.d_stride, Elem<DT>::kSize);
+    rr.x = x;
+    const uintptr_t ga = (uintptr_t)(rp + (int64_t)x * Elem<DT>::kSize);
+    rr.zx = SSD_CHK(in_range(ga, ga + Elem<DT>::kSize, it ? p.t_lo : p.d_lo, it ? p.t_hi : p.d_hi),
+                    p.dbg, 4, row, x) ? Elem<DT>::load_cg(rp, x) : 0.f;
+  }
+  if (lane == 0 && SSD_CHK(row < p.NR, p.dbg, 5, row, p.NR)) p.rowres[row] = rr;
+  // bonus guesses: top-(F_j+1) minus the sampled token, truncated to F_j
+  if (!is_t && p.guesses != nullptr && lane == 0) {
+    const int F = p.F[j];
+    int n = 0;
+    const int64_t o = (g * p.nd + j) * (int64_t)p.Fmax;
+    for (int k = 0; k < kMaxTopK && n < F; ++k) {
+      if (rr.ti[k] < 0 || rr.ti[k] == rr.x) continue;
+      if (!SSD_CHK(o + n < (int64_t)p.B * p.nd * p.Fmax && n < p.Fmax, p.dbg, 7, o + n, n)) break;
+      p.guesses[o + n] = rr.ti[k];
+      if (p.guess_q) p.guess_q[o + n] = (float)((double)exp2f(fmaf(rr.tv[k], p.c, -MC)) / rr.s);
+      ++n;
+    }
+    for (; n < p.Fmax; ++n) {
+      if (!SSD_CHK(o + n < (int64_t)p.B * p.nd * p.Fmax, p.dbg, 7, o + n, n)) break;
+      p.guesses[o + n] = -1;
+      if (p.guess_q) p.guess_q[o + n] = 0.f;
+    }
+  }
+  if (p.mode == kModeTopF) return;
+  // sequence arrival
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();
+    last = SSD_CHK(g < p.B, p.dbg, 9, g, p.B) ? atomicAdd(p.grp_cnt + g, 1) == p.rpg - 1 : 0;
+    if (last) __threadfence();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  if (p.mode == kModeVerify) {
+    verify_epilogue(p, g);
+  } else if (lane == 0) {
+    saguaro_epilogue(p, g, rr);
+  }
+}
+
+template <int DT, int TOPK>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamParams p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesA * kStageBytes);
+  uint64_t* empty = full + kStagesA;
+  PieceRed<TOPK>* red = reinterpret_cast<PieceRed<TOPK>*>(empty + kStagesA);  // [2]
+  __shared__ int s_err;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t u_begin = (int64_t)blockIdx.x * p.upc;
+  const int64_t u_end = min(u_begin + p.upc, p.total_units);
+  if (u_begin >= u_end) return;
+  constexpr int ups = kStageBytes / (kUnitA * Elem<DT>::kSize);  // units per stage
+
+  if (tid == 0) {
+    for (int i = 0; i < kStagesA; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kConsumerWarps);
+    }
+    s_err = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      int n = 0;
+      for (int64_t u = u_begin; u < u_end;) {
+        const int64_t row = u / p.upr;
+        const int64_t ure = min((row + 1) * p.upr, u_end);
+        for (int64_t un = 0; u < ure; u = un) {
+          un = min(u + ups, ure);
+          const Stage st = stage_geometry<DT>(p, row, u, un);
+          const int slot = n % kStagesA;
+          if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+          const uint32_t bytes = (uint32_t)(st.a1 - st.a0);
+          const bool tsrc = (row % p.rpg) < p.nt;
+          if (bytes > 0 && !s_err &&
+              SSD_CHK(in_range(st.a0, st.a1, tsrc ? p.t_lo : p.d_lo, tsrc ? p.t_hi : p.d_hi),
+                      p.dbg, 1, st.a0, st.a1)) {
+            mbar_arrive_expect_tx(full + slot, bytes);
+            bulk_g2s(ring + slot * kStageBytes, reinterpret_cast<const void*>(st.a0), bytes,
+                     full + slot);
+          } else {
+            mbar_arrive(full + slot);
+          }
+          ++n;
+        }
+      }
+      // do not leave while copies into this CTA's shared memory are in flight
+      for (int q = max(0, n - kStagesA); q < n; ++q)
+        mbar_wait(full + (q % kStagesA), (q / kStagesA) & 1, &s_err, p.status);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const float c = p.c;
+  Acc<TOPK> a;
+  int n = 0;
+  int piece = 0;
+  for (int64_t u = u_begin; u < u_end; ++piece) {
+    const int64_t row = u / p.upr;
+    const int64_t ure = min((row + 1) * p.upr, u_end);
+    const int64_t g = row / p.rpg;
+    const int jr = (int)(row - g * p.rpg);
+    const bool is_t = jr < p.nt;
+    const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
+    a.reset();
+    for (int64_t un = 0; u < ure; u = un) {
+      un = min(u + ups, ure);
+      const Stage st = stage_geometry<DT>(p, row, u, un);
+      const int slot = n % kStagesA;
+      mbar_wait(full + slot, (n / kStagesA) & 1, &s_err, p.status);
+      const int nvec = (int)((st.a1 - st.a0) >> 4);
+      const int ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
+      const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
+#pragma unroll 4
+      for (int v = tid; v < nvec; v += kConsumers)
+        if (SSD_CHK(v < kStageBytes / 16, p.dbg, 10, v, nvec))
+          consume_vec<DT, TOPK>(a, sv[v], ei0 + v * Elem<DT>::kVec, c, top);
+      // unaligned head / tail elements straight from global memory
+      const int hc = nvec > 0 ? (int)((st.a0 - st.b0) / Elem<DT>::kSize) : st.e1 - st.e0;
+      const int ei1 = ei0 + nvec * Elem<DT>::kVec;
+      const int tc = nvec > 0 ? st.e1 - ei1 : 0;
+      for (int f = tid; f < hc + tc; f += kConsumers) {
+        const int idx = f < hc ? st.e0 + f : ei1 + (f - hc);
+        const uintptr_t fa = st.b0 + (uintptr_t)(idx - st.e0) * Elem<DT>::kSize;
+        const bool tsrc = is_t;
+        if (!SSD_CHK(in_range(fa, fa + Elem<DT>::kSize, tsrc ? p.t_lo : p.d_lo,
+                              tsrc ? p.t_hi : p.d_hi), p.dbg, 2, idx, st.e0))
+          continue;
+        const float x = Elem<DT>::load(reinterpret_cast<const void*>(st.b0),
+                                       (int64_t)(idx - st.e0));
+        consume_one<TOPK>(a, x, idx, c, top);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + slot);
+      ++n;
+    }
+
+    // ---- piece reduction: warp, then CTA ----
+    float M, MC, Shi, Slo;
+    warp_softmax_merge(a.m, a.mc, a.hi, a.lo, c, M, MC, Shi, Slo);
+    if constexpr (TOPK > 0) {
+      if (top) warp_topk_merge<TOPK>(a.tv, a.ti);
+    }
+    PieceRed<TOPK>& R = red[piece & 1];
+    if (lane == 0) {
+      R.m[warp] = M;
+      R.hi[warp] = Shi;
+      R.lo[warp] = Slo;
+#pragma unroll
+      for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
+        R.tv[warp][k] = a.tv[k];
+        R.ti[warp][k] = a.ti[k];
+      }
+    }
+    consumer_sync();
+    if (warp != 0) continue;
+
+    // warp 0: combine the eight warp results
+    Acc<TOPK> b;
+    b.reset();
+    if (lane < kConsumerWarps) {
+      b.m = R.m[lane];
+      b.mc = b.m == kNegInf ? kNegInf : __fmul_rn(b.m, c);
+      b.hi = R.hi[lane];
+      b.lo = R.lo[lane];
+      if (TOPK > 0 && top) {
+#pragma unroll
+        for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
+          b.tv[k] = R.tv[lane][k];
+          b.ti[k] = R.ti[lane][k];
+        }
+      }
+    }
+    warp_softmax_merge(b.m, b.mc, b.hi, b.lo, c, M, MC, Shi, Slo);
+    if constexpr (TOPK > 0) {
+      if (top) warp_topk_merge<TOPK>(b.tv, b.ti);
+    }
+
+    const int64_t r0u = row * p.upr;
+    const int64_t c_lo = r0u / p.upc;
+    const int64_t c_hi = (r0u + p.upr - 1) / p.upc;
+    if (c_lo == c_hi) {
+      finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, b, top);
+      continue;
+    }
+    // row shared with other CTAs: publish the partial, last arrival merges
+    if (!SSD_CHK(row + blockIdx.x < p.NR + kMaxGrid && row < p.NR, p.dbg, 6, row, blockIdx.x))
+      continue;
+    RowPartial* slotp = p.partials + (row + blockIdx.x);
+    if (lane == 0) {
+      slotp->m = M;
+      slotp->s_hi = Shi;
+      slotp->s_lo = Slo;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
+        slotp->tv[k] = (TOPK > 0 && top) ? b.tv[k] : kNegInf;
+        slotp->ti[k] = (TOPK > 0 && top) ? b.ti[k] : 0x7fffffff;
+      }
+    }
+    int last = 0;
+    if (lane == 0) {
+      __threadfence();
+      last = atomicAdd(p.row_cnt + row, 1) == (int)(c_hi - c_lo);
+      if (last) __threadfence();
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    Acc<TOPK> mrg;
+    mrg.reset();
+    for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32)
+      fold_partial<TOPK>(mrg, p.partials + (row + cc), c, top);
+    warp_softmax_merge(mrg.m, mrg.mc, mrg.hi, mrg.lo, c, M, MC, Shi, Slo);
+    if constexpr (TOPK > 0) {
+      if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti);
+    }
+    finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, mrg, top);
+  }
+}
+
+template <int DT, int TOPK>
+cudaError_t launch_t(const StreamParams& p, int grid, cudaStream_t s) {
+  const int smem = stream_smem_bytes();
+  auto kern = stream_kernel<DT, TOPK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(const StreamParams& p, int topk, int grid, cudaStream_t s) {
+  switch (topk) {
+    case 0: return launch_t<DT, 0>(p, grid, s);
+    case 2: return launch_t<DT, 2>(p, grid, s);
+    case 4: return launch_t<DT, 4>(p, grid, s);
+    case 8: return launch_t<DT, 8>(p, grid, s);
+    case 16: return launch_t<DT, 16>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int stream_smem_bytes() {
+  return kStagesA * kStageBytes + 2 * kStagesA * (int)sizeof(uint64_t) +
+         2 * (int)sizeof(PieceRed<kMaxTopK>);
+}
+
+cudaError_t launch_stream(const StreamParams& p, int dtype, int topk, int grid, cudaStream_t s) {
+  return dtype == SSD_BF16 ? launch_dt<0>(p, topk, grid, s) : launch_dt<1>(p, topk, grid, s);
+}
+
+}  // namespace ssd

@@ -1,0 +1,232 @@
+"""GPU parity of ssd_verify against the CPU oracle, through the C ABI.
+
+Sources (page title, section): [SD-7.3] "7.3 Speculative Decoding：投机采样加速"
+§7.3.2-7.3.3; [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个
+顺序瓶颈" §"Saguaro 优化二：Saguaro 采样", §"怎么猜奖励 token".
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import sampling_ssd_verify_gb300 as ssd
+from ssd_inputs import WORKLOADS, make_batch
+from tests.parity import compare_verify, i32, seeds_t, to_np, torch_dev, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ssd.build()
+    ssd.lib()
+
+
+def _padded(arr, dtype, pad):
+    """Upload [B, R, V] with `pad` extra elements per row (row stride V+pad)."""
+    torch, dev = torch_dev()
+    if pad == 0:
+        return upload(arr, dtype)
+    B, R, V = arr.shape
+    big = np.zeros((B, R, V + pad), dtype=arr.dtype)
+    big[:, :, :V] = arr
+    return upload(big, dtype)[:, :, :V]
+
+
+def run_verify(orc, w, B=None, V=None, K=None, dtype=None, rounds=(0,), seed=None, C=None,
+               T=None, F=None, Kq=None, pad=0, offset=0, nthreads=16, batch=None):
+    torch, dev = torch_dev()
+    bt = batch if batch is not None else make_batch(w, B=B, V=V, K=K, seed=seed, dtype=dtype)
+    K = bt["K"]
+    dtype = bt["dtype"]
+    C = w.C if C is None else C
+    T = w.T if T is None else T
+    Kq = K + 1 if Kq is None else Kq
+    F = np.asarray(w.fanout if F is None else F, dtype=np.int32)[:Kq]
+    target = bt["target"]
+    draft = np.ascontiguousarray(bt["draft"][:, :Kq])
+    seeds = bt["seeds"]
+    if offset:
+        # shift the whole batch by `offset` elements inside a larger buffer
+        flat_t = np.concatenate([np.zeros(offset, target.dtype), target.ravel()])
+        flat_d = np.concatenate([np.zeros(offset, draft.dtype), draft.ravel()])
+        tg = upload(flat_t, dtype)[offset:].view(target.shape)
+        dg = upload(flat_d, dtype)[offset:].view(draft.shape)
+    else:
+        tg = _padded(target, dtype, pad)
+        dg = _padded(draft, dtype, pad)
+    stats_all = []
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for r in rounds:
+        tok = orc.draft_tokens(draft, F, C, T, seeds, round_=r, K=K, nthreads=nthreads)
+        g = ssd.verify(tg, dg, i32(tok), seeds_t(seeds), r, F, C, T, dev_status=status)
+        torch.cuda.synchronize()
+        o = orc.verify(target, draft, tok, seeds, r, F, C, T, Fmax=max(1, int(F.max())),
+                       nthreads=nthreads)
+        stats_all.append(compare_verify(to_np(g), o, K))
+    assert int(status.item()) == 0
+    return stats_all
+
+
+def test_c1_tiny_exactness_many_rows(orc):
+    """B=1,K=4,V=32 fp32 (C=0.5, F=[3,3,2,2,2]) drawn for 20000 independent
+    sequences x 5 rounds."""
+    w = WORKLOADS["c1"]
+    st = run_verify(orc, w, B=20000, rounds=range(5))
+    assert sum(s["rows"] for s in st) == 100000
+
+
+def test_c2_single_stream_llama_vocab(orc):
+    """B=1, K=4, V=128256 bf16, T=0.7, C=0.5: 24 seeded rounds."""
+    w = WORKLOADS["c2"]
+    run_verify(orc, w, rounds=range(24))
+
+
+def test_c3_batched_full_size(orc):
+    """B=64, K=8, V=128256 bf16, C=1, budget 16: every row against the oracle."""
+    w = WORKLOADS["c3"]
+    st = run_verify(orc, w, rounds=(0, 1))
+    for s in st:
+        assert 0.5 < s["accept_mean"] < 8
+
+
+def test_c4_outer_verify(orc):
+    """The SSD round's verify of 32 outer rows: K=4, V=151936 bf16, C=0.3."""
+    w = WORKLOADS["c4"]
+    run_verify(orc, w, rounds=(3,))
+
+
+def test_c5_large_batch_sampled_rows(orc):
+    """B=256, K=8, V=151936 fp32, C=0.5, budget 24 at full size, in the launch
+    configuration the benchmark times; the oracle checks a sample of rows."""
+    torch, dev = torch_dev()
+    w = WORKLOADS["c5"]
+    bt = make_batch(w)
+    K, Kq = w.K, w.Kq
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], round_=5, K=K, nthreads=16)
+    tg = upload(bt["target"], "f32")
+    dg = upload(bt["draft"], "f32")
+    g = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 5, F, w.C, w.T))
+    rows = np.array([0, 1, 17, 63, 64, 100, 127, 128, 200, 254, 255])
+    o = orc.verify(bt["target"][rows], bt["draft"][rows], tok[rows], bt["seeds"][rows], 5, F,
+                   w.C, w.T, nthreads=16, row_ids=rows)
+    compare_verify({kk: v[rows] for kk, v in g.items()}, o, K)
+    # properties every row must satisfy
+    assert np.all((g["accept_len"] >= 0) & (g["accept_len"] <= K))
+    assert np.all((g["bonus"] >= 0) & (g["bonus"] < w.V))
+    rej = g["accept_len"] < K
+    assert np.all(g["bonus"][rej] != tok[rej, g["accept_len"][rej]])
+    assert np.all((g["resid_mass"] > 0) & (g["resid_mass"] <= 1 + 1e-5))
+
+
+@dataclasses.dataclass
+class Edge:
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    F: tuple
+    C: float = 0.5
+    T: float = 1.0
+    Kq: int | None = None
+    pad: int = 0
+    offset: int = 0
+
+
+EDGES = [
+    Edge("V37 unaligned rows f32", 50, 3, 37, "f32", (2, 2, 1, 1)),
+    Edge("V37 unaligned rows bf16", 50, 3, 37, "bf16", (2, 2, 1, 1)),
+    Edge("V2 minimum vocab", 200, 1, 2, "f32", (1, 0), C=0.3),
+    Edge("K1 no fan-out", 100, 1, 300, "bf16", (0, 0), C=0.4),
+    Edge("K32 maximum drafts", 4, 32, 515, "f32", tuple([1] * 33)),
+    Edge("Kq=K no draft row K", 40, 4, 1000, "bf16", (3, 2, 2, 1), Kq=4),
+    Edge("padded row stride f32", 20, 4, 3001, "f32", (3, 3, 2, 2, 2), pad=5),
+    Edge("padded row stride bf16", 20, 4, 3001, "bf16", (3, 3, 2, 2, 2), pad=3),
+    Edge("odd element offset bf16", 8, 4, 4099, "bf16", (3, 3, 2, 2, 2), offset=1),
+    Edge("rows split over many CTAs", 3, 7, 20000, "f32", (5, 4, 3, 3, 2, 2, 1, 1)),
+    Edge("F up to 15", 6, 2, 700, "bf16", (15, 9, 4), C=0.2),
+    Edge("high temperature", 30, 4, 2048, "f32", (3, 3, 2, 2, 2), T=2.5),
+    Edge("low temperature", 30, 4, 2048, "bf16", (3, 3, 2, 2, 2), T=0.3),
+]
+
+
+@pytest.mark.parametrize("e", EDGES, ids=[e.name for e in EDGES])
+def test_edge_shapes(orc, e):
+    w = dataclasses.replace(WORKLOADS["c2"], gen="G" if e.V > 64 else "gauss", T=e.T,
+                            fanout=e.F, C=e.C, seed=77)
+    run_verify(orc, w, B=e.B, V=e.V, K=e.K, dtype=e.dtype, rounds=(0, 1), F=e.F, Kq=e.Kq,
+               pad=e.pad, offset=e.offset)
+
+
+def test_plain_sd_is_bit_identical_with_c1_or_empty_sets(orc):
+    """C = 1 (any F) and F = 0 (any C) are both plain speculative decoding:
+    identical accept lengths, bonus tokens and residual masses."""
+    torch, dev = torch_dev()
+    w = WORKLOADS["c3"]
+    bt = make_batch(w, B=16, V=20000)
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tok = orc.draft_tokens(bt["draft"], np.zeros_like(F), 1.0, w.T, bt["seeds"], K=w.K)
+    tg, dg = upload(bt["target"], "bf16"), upload(bt["draft"], "bf16")
+    a = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 0, F, 1.0, w.T))
+    b = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 0, np.zeros_like(F), 0.4, w.T,
+                         guesses=False))
+    for k in ("accept_len", "bonus", "resid_mass"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_bad_token_sets_status(orc):
+    torch, dev = torch_dev()
+    w = WORKLOADS["c1"]
+    bt = make_batch(w, B=4)
+    tok = np.zeros((4, w.K), dtype=np.int32)
+    tok[2, 1] = w.V + 5
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ssd.verify(upload(bt["target"], "f32"), upload(bt["draft"], "f32"), i32(tok),
+               seeds_t(bt["seeds"]), 0, w.fanout, w.C, w.T, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & ssd.DEV_BAD_TOKEN
+
+
+def test_gpu_laws_chi_square(orc):
+    """The library's own outputs follow the exact laws: accept length
+    P(k >= j) = prod alpha_i and bonus ~ normalize((p_i - q'_i)^+) (or p_K),
+    over 10^6 seeded trials at V = 32."""
+    torch, dev = torch_dev()
+    rng = np.random.default_rng(31)
+    K, V, C, T = 2, 32, 0.5, 1.0
+    zp = rng.normal(0, 1.0, (K + 1, V)).astype(np.float32)
+    zq = (zp + rng.normal(0, 0.7, (K + 1, V))).astype(np.float32)
+    F = np.array([3, 2, 2], dtype=np.int32)
+    p = [orc.softmax(zp[i], T) for i in range(K + 1)]
+    qp = [orc.saguaro_dist(zq[j], T, int(F[j]), C) for j in range(K)]
+    n = 250_000
+    tgt = np.ascontiguousarray(np.broadcast_to(zp, (n, K + 1, V)))
+    dft = np.ascontiguousarray(np.broadcast_to(zq, (n, K + 1, V)))
+    seeds = np.arange(n, dtype=np.uint64) * 7 + 5
+    tg, dg = upload(tgt, "f32"), upload(dft, "f32")
+    ks, ts = [], []
+    for r in range(4):
+        tok = orc.draft_tokens(dft, F, C, T, seeds, round_=r, K=K, nthreads=16)
+        g = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(seeds), r, F, C, T, guesses=False))
+        ks.append(g["accept_len"])
+        ts.append(g["bonus"])
+    ks, ts = np.concatenate(ks), np.concatenate(ts)
+    alpha = [np.minimum(p[i], qp[i]).sum() for i in range(K)]
+    ge = np.cumprod([1.0] + alpha)
+    pk = np.append(ge[:-1] - ge[1:], ge[K])
+    assert stats.chisquare(np.bincount(ks, minlength=K + 1), pk * len(ks)).pvalue > 1e-4
+    for i in range(K + 1):
+        sel = ts[ks == i]
+        if i < K:
+            wr, Z = orc.residual(p[i], qp[i])
+            expect = wr / Z
+        else:
+            expect = p[K]
+        obs = np.bincount(sel, minlength=V)
+        m = expect * len(sel) > 5
+        st = stats.chisquare(obs[m], expect[m] / expect[m].sum() * obs[m].sum())
+        assert st.pvalue > 1e-4, (i, st)
