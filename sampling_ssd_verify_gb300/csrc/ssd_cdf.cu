@@ -29,8 +29,6 @@ namespace ssd {
 
 namespace {
 
-constexpr float kPosInf = INFINITY;
-
 // One row half of a stage: where element y lives (shared memory or global).
 struct Half {
   const char* row;   // row base (global)
@@ -133,9 +131,41 @@ __device__ int full_row_draw(const CdfParams& p, const GroupParams& gp, const ch
   return t;
 }
 
+// Sixteen consecutive logits of row `r` starting at y0 (< e1), vectorised
+// when the address is 16-byte aligned and the run is complete.
+template <int DT>
+__device__ __forceinline__ void load16(const CdfParams& p, const char* r, bool is_t, int y0,
+                                       int e1, float* z) {
+  constexpr int ES = Elem<DT>::kSize;
+  constexpr int VEC = Elem<DT>::kVec;
+  const uintptr_t a = (uintptr_t)(r + (int64_t)y0 * ES);
+  if (y0 + 16 <= e1 && (a & 15) == 0 &&
+      SSD_CHK(in_range(a, a + 16 * ES, is_t ? p.t_lo : p.d_lo, is_t ? p.t_hi : p.d_hi), p.dbg, 29,
+              y0, e1)) {
+    const uint4* v = reinterpret_cast<const uint4*>(a);
+#pragma unroll
+    for (int k = 0; k < 16 / VEC; ++k) Elem<DT>::unpack(__ldg(v + k), z + k * VEC);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int y = y0 + k;
+      const uintptr_t ay = (uintptr_t)(r + (int64_t)y * ES);
+      z[k] = (y < e1 && SSD_CHK(in_range(ay, ay + ES, is_t ? p.t_lo : p.d_lo,
+                                         is_t ? p.t_hi : p.d_hi), p.dbg, 29, y, e1))
+                 ? Elem<DT>::load(r, y) : 0.f;
+    }
+  }
+}
+
 // The draw for group g (warp 0 of the last CTA to finish the group).
+// 1. Z = sum of the group's unit sums (each lane loads 16 units at once).
+// 2. The unit holding u*Z: lane prefix in registers + warp scan (fp64).
+// 3. Inside that unit: each lane takes 16 consecutive tokens, lane prefix +
+//    warp scan in vocabulary order; the first token whose cumulative weight
+//    exceeds the remainder is the draw.
 template <int DT>
 __device__ void group_draw(const CdfParams& p, int64_t g) {
+  constexpr int R = 16;  // unit sums per lane per round
   const int lane = threadIdx.x & 31;
   if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) return;
   const GroupParams gp = p.gp[g];
@@ -143,15 +173,26 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, esz) : nullptr;
   const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, esz) : nullptr;
   const float* sub = p.subsum + g * p.nsub;
-  const int per = (p.nsub + 31) / 32;
-  const int lo = min(lane * per, p.nsub);
-  const int hi = min(lo + per, p.nsub);
-  double loc = 0.0;
-  for (int u = lo; u < hi; ++u)
-    if (SSD_CHK(g * p.nsub + u < (int64_t)p.groups * p.nsub, p.dbg, 23, g, u))
-      loc += (double)__ldcg(sub + u);
-  const double incl = warp_incl_scan(loc);
-  double Z = __shfl_sync(0xffffffffu, incl, 31);
+  const int nsub = p.nsub;
+  const int rounds = (nsub + 32 * R - 1) / (32 * R);
+  float v[R];
+  auto load_round = [&](int rnd) {
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const int u = rnd * 32 * R + lane * R + k;
+      v[k] = (u < nsub && SSD_CHK(g * nsub + u < (int64_t)p.groups * nsub, p.dbg, 23, g, u))
+                 ? __ldcg(sub + u) : 0.f;
+    }
+  };
+  double Zl = 0.0;
+  for (int rnd = 0; rnd < rounds; ++rnd) {
+    load_round(rnd);
+#pragma unroll
+    for (int k = 0; k < R; ++k) Zl += (double)v[k];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Zl += __shfl_xor_sync(0xffffffffu, Zl, off);
+  double Z = Zl;
   int t;
   float wt;
   if (!(Z > 1e-30)) {
@@ -160,7 +201,6 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
     if (lane == 0 && p.status) atomicOr(p.status, SSD_DEV_ZERO_RESIDUAL);
     GroupParams gp2 = gp;
     gp2.use_d = 0;
-    gp2.use_t = gp.use_t;
     if (!gp2.use_t) {  // Saguaro rows always have Z ~ 1; keep a defined result
       gp2.use_d = 1;
       gp2.sign_d = 1;
@@ -169,55 +209,112 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
     wt = weight_global<DT>(p, gp2, rt, rd, t);
   } else {
     const double thr = gp.u * Z;
-    const unsigned m = __ballot_sync(0xffffffffu, incl > thr && lo < hi);
     int unit = -1;
     double before = 0.0;
-    if (m) {
-      const int L = __ffs(m) - 1;
-      if (lane == L) {
-        double run = incl - loc;
-        for (int u = lo; u < hi; ++u) {
-          const double nx = run + (double)__ldcg(sub + u);
-          if (nx > thr) {
-            unit = u;
-            before = run;
-            break;
-          }
-          run = nx;
-        }
-        if (unit < 0) {  // rounding: the lane's own running sum never exceeded thr;
-                         // fall back to the last positive weight of its range
-          for (int u = hi - 1; u >= lo; --u)
-            if (__ldcg(sub + u) > 0.f) {
-              unit = u;
-              break;
+    double run = 0.0;
+    for (int rnd = 0; rnd < rounds && unit < 0; ++rnd) {
+      if (rounds > 1) load_round(rnd);
+      double loc = 0.0;
+#pragma unroll
+      for (int k = 0; k < R; ++k) loc += (double)v[k];
+      const double incl = warp_incl_scan(loc);
+      const unsigned m = __ballot_sync(0xffffffffu, run + incl > thr);
+      if (m) {
+        const int L = __ffs(m) - 1;
+        int uk = -1;
+        double bk = 0.0;
+        if (lane == L) {
+          double acc = run + (incl - loc);
+#pragma unroll
+          for (int k = 0; k < R; ++k) {
+            if (uk < 0 && v[k] > 0.f && acc + (double)v[k] > thr) {
+              uk = k;
+              bk = acc;
             }
-          before = -INFINITY;
+            acc += (double)v[k];
+          }
+          if (uk < 0) {  // rounding inside the lane: its last positive unit
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+              if (v[k] > 0.f) uk = k;
+            bk = -INFINITY;
+          }
+        }
+        uk = __shfl_sync(0xffffffffu, uk, L);
+        bk = __shfl_sync(0xffffffffu, bk, L);
+        if (uk >= 0) {
+          unit = rnd * 32 * R + L * R + uk;
+          before = bk;
         }
       }
-      unit = __shfl_sync(0xffffffffu, unit, L);
-      before = __shfl_sync(0xffffffffu, before, L);
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (unit < 0) {  // no prefix exceeded u*Z: take the last unit with weight
+    if (unit < 0) {  // no prefix exceeded u*Z: the last unit with weight
       int cand = -1;
-      for (int u = hi - 1; u >= lo; --u)
-        if (__ldcg(sub + u) > 0.f) {
-          cand = u;
-          break;
-        }
+      for (int rnd = 0; rnd < rounds; ++rnd) {
+        load_round(rnd);
+#pragma unroll
+        for (int k = 0; k < R; ++k)
+          if (v[k] > 0.f) cand = rnd * 32 * R + lane * R + k;
+      }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1)
         cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
-      unit = cand >= 0 ? cand : p.nsub - 1;
+      unit = cand >= 0 ? cand : nsub - 1;
       before = -INFINITY;  // no index qualifies: the last positive weight is taken
     }
+    // vocabulary-order scan of the unit: lane l holds tokens e0 + 16 l ...
     const int e0 = unit * kUnitB;
     const int e1 = min(e0 + kUnitB, p.V);
-    double run = 0.0;
-    int last = -1;
-    t = scan_range<DT>(p, gp, rt, rd, e0, e1, thr - before, &run, &last);
-    if (t < 0) t = last >= 0 ? last : e0;
-    wt = weight_global<DT>(p, gp, rt, rd, t);
+    const int y0 = e0 + lane * 16;
+    float zt[16], zd[16], w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) zt[k] = zd[k] = 0.f;
+    if (gp.use_t) load16<DT>(p, rt, true, y0, e1, zt);
+    if (gp.use_d) load16<DT>(p, rd, false, y0, e1, zd);
+    double loc = 0.0;
+    int lastpos = -1;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      w[k] = y0 + k < e1 ? weight(gp, p.c, y0 + k, zt[k], zd[k]) : 0.f;
+      loc += (double)w[k];
+      if (w[k] > 0.f) lastpos = y0 + k;
+    }
+    const double incl = warp_incl_scan(loc);
+    const double rem = thr - before;
+    const unsigned m = __ballot_sync(0xffffffffu, incl > rem);
+    t = -1;
+    wt = 0.f;
+    if (m) {
+      const int L = __ffs(m) - 1;
+      int tk = -1;
+      if (lane == L) {
+        double acc = incl - loc;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          if (tk < 0 && w[k] > 0.f && acc + (double)w[k] > rem) tk = k;
+          acc += (double)w[k];
+        }
+        if (tk < 0)
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (w[k] > 0.f) tk = k;
+      }
+      tk = __shfl_sync(0xffffffffu, tk, L);
+      if (tk >= 0) t = e0 + L * 16 + tk;
+    }
+    if (t < 0) {  // rounding left no index: the last positive weight of the unit
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
+      t = lastpos >= 0 ? lastpos : e0;
+    }
+    const int owner = (t - e0) >> 4;
+    float wown = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if (y0 + k == t) wown = w[k];
+    wt = __shfl_sync(0xffffffffu, wown, owner & 31);
   }
   if (lane != 0) return;
   if (!SSD_CHK(g < p.groups && t >= 0 && t < p.V, p.dbg, 25, g, t)) return;
@@ -237,11 +334,47 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   }
 }
 
+// Ring geometry of the CDF pass: a stage holds kUnitsPerStageB units of the
+// target row and of the draft row.
+template <int DT>
+struct CdfRing {
+  static constexpr int ES = Elem<DT>::kSize;
+  static constexpr int HALF = kUnitsPerStageB * kUnitB * ES;
+  static constexpr int STAGE = 2 * HALF;
+  static constexpr int NST = kRingBytesB / STAGE;
+};
+
+// Sum of the draw weights of one whole unit whose elements sit 16-byte
+// aligned in shared memory (vectorised fast path of one warp).
+template <int DT>
+__device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupParams& gp,
+                                               const Half& ht, const Half& hd, int ue0) {
+  constexpr int VEC = Elem<DT>::kVec;
+  constexpr int NV = kUnitB / VEC / 32;
+  const int lane = threadIdx.x & 31;
+  const uint4* st4 = reinterpret_cast<const uint4*>(ht.sm + (ue0 - ht.ei0) * Elem<DT>::kSize);
+  const uint4* sd4 = reinterpret_cast<const uint4*>(hd.sm + (ue0 - hd.ei0) * Elem<DT>::kSize);
+  float s = 0.f;
+#pragma unroll
+  for (int m = 0; m < NV; ++m) {
+    const int vi = lane + 32 * m;
+    float zt[VEC], zd[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) zt[e] = zd[e] = 0.f;
+    if (gp.use_t) Elem<DT>::unpack(st4[vi], zt);
+    if (gp.use_d) Elem<DT>::unpack(sd4[vi], zd);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) s += weight(gp, p.c, ue0 + vi * VEC + e, zt[e], zd[e]);
+  }
+  return s;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) cdf_kernel(const __grid_constant__ CdfParams p) {
   constexpr int ES = Elem<DT>::kSize;
-  constexpr int HALF = kUnitsPerStageB * kUnitB * ES;
-  constexpr int STAGE = 2 * HALF;
+  constexpr int HALF = CdfRing<DT>::HALF;
+  constexpr int STAGE = CdfRing<DT>::STAGE;
+  constexpr int kStagesB = CdfRing<DT>::NST;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesB * STAGE);
@@ -353,22 +486,27 @@ __global__ void __launch_bounds__(kThreads, 1) cdf_kernel(const __grid_constant_
       if (uu < un) {
         const int ue0 = (int)((uu - g * p.nsub) * kUnitB);
         const int ue1 = min(ue0 + kUnitB, p.V);
+        constexpr int VEC = Elem<DT>::kVec;
+        bool fast = ue1 - ue0 == kUnitB;
+        if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
+        if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
         float s = 0.f;
-#pragma unroll 4
-        for (int m = 0; m < kUnitB / 32; ++m) {
-          const int y = ue0 + lane + 32 * m;
-          if (y < ue1) {
-            const float zt = gp.use_t ? fetch<DT>(ht, y, p, true) : 0.f;
-            const float zd = gp.use_d ? fetch<DT>(hd, y, p, false) : 0.f;
-            s += weight(gp, p.c, y, zt, zd);
+        if (fast) {
+          s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
+        } else {
+          for (int m = 0; m < kUnitB / 32; ++m) {
+            const int y = ue0 + lane + 32 * m;
+            if (y < ue1) {
+              const float zt = gp.use_t ? fetch<DT>(ht, y, p, true) : 0.f;
+              const float zd = gp.use_d ? fetch<DT>(hd, y, p, false) : 0.f;
+              s += weight(gp, p.c, y, zt, zd);
+            }
           }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0 && SSD_CHK(uu < (int64_t)p.groups * p.nsub, p.dbg, 23, uu, g)) {
+        if (lane == 0 && SSD_CHK(uu < (int64_t)p.groups * p.nsub, p.dbg, 23, uu, g))
           p.subsum[g * p.nsub + (uu - g * p.nsub)] = s;
-          __threadfence();
-        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + slot);
@@ -394,8 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1) cdf_kernel(const __grid_constant_
 }  // namespace
 
 int cdf_smem_bytes(int dtype) {
-  const int es = dtype == SSD_BF16 ? 2 : 4;
-  return kStagesB * 2 * kUnitsPerStageB * kUnitB * es + 2 * kStagesB * (int)sizeof(uint64_t);
+  return dtype == SSD_BF16
+             ? CdfRing<0>::NST * CdfRing<0>::STAGE + 2 * CdfRing<0>::NST * (int)sizeof(uint64_t)
+             : CdfRing<1>::NST * CdfRing<1>::STAGE + 2 * CdfRing<1>::NST * (int)sizeof(uint64_t);
 }
 
 cudaError_t launch_cdf(const CdfParams& p, int dtype, int grid, cudaStream_t s) {

@@ -15,15 +15,15 @@
 namespace ssd {
 
 // ---- tuning ------------------------------------------------------------------
-constexpr int kConsumerWarps = 8;                   // warps that reduce staged data
+constexpr int kConsumerWarps = 16;                  // warps that reduce staged data
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;           // + one producer (bulk-copy) warp
 constexpr int kUnitA = 1024;                        // elements per work unit, streaming pass
-constexpr int kStageBytes = 16384;                  // bytes per pipeline stage
-constexpr int kStagesA = 8;                         // ring depth, streaming pass
+constexpr int kStageBytes = 32768;                  // bytes per pipeline stage
+constexpr int kStagesA = 6;                         // ring depth, streaming pass
 constexpr int kUnitB = 512;                         // elements per unit, CDF pass
 constexpr int kUnitsPerStageB = kConsumerWarps;     // one unit per consumer warp
-constexpr int kStagesB = 4;                         // ring depth, CDF pass
+constexpr int kRingBytesB = 196608;                // bulk-copy ring of the CDF pass
 constexpr int kMaxTopK = 16;                        // per-row candidate list (F + 1 <= 16)
 constexpr int kMaxGrid = 4096;                      // bound on CTAs of one launch
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s

@@ -47,7 +47,6 @@ struct alignas(16) PieceRed {
 // Geometry of one pipeline stage: the element range [e0, e1) of row `row`
 // and its 16-byte-aligned interior [a0, a1) (byte addresses).
 struct Stage {
-  int64_t row;
   int e0, e1;
   uintptr_t b0, a0, a1;
 };
@@ -66,21 +65,31 @@ __device__ __forceinline__ const void* tensor_of(const StreamParams& p, int64_t 
   return p.dft;
 }
 
+// Row-level geometry, computed once per row piece.
+struct RowGeom {
+  const char* rp;  // address of element 0 of the row
+  int64_t ur;      // first unit of the row in the flattened unit space
+  bool is_t;       // target row (else draft row)
+};
+
 template <int DT>
-__device__ __forceinline__ Stage stage_geometry(const StreamParams& p, int64_t row, int64_t u,
-                                                int64_t un) {
-  Stage st;
-  st.row = row;
-  const int64_t ur = row * p.upr;
-  st.e0 = (int)((u - ur) * kUnitA);
-  st.e1 = (int)min((int64_t)p.V, (un - ur) * kUnitA);
+__device__ __forceinline__ RowGeom row_geom(const StreamParams& p, int64_t row) {
+  RowGeom rg;
   int64_t trow;
-  bool is_t;
-  const void* base = tensor_of<DT>(p, row, trow, is_t);
-  const int64_t stride = is_t ? p.t_stride : p.d_stride;
-  const char* rp = row_ptr(base, trow, stride, Elem<DT>::kSize);
-  st.b0 = (uintptr_t)(rp + (int64_t)st.e0 * Elem<DT>::kSize);
-  const uintptr_t b1 = (uintptr_t)(rp + (int64_t)st.e1 * Elem<DT>::kSize);
+  const void* base = tensor_of<DT>(p, row, trow, rg.is_t);
+  rg.rp = row_ptr(base, trow, rg.is_t ? p.t_stride : p.d_stride, Elem<DT>::kSize);
+  rg.ur = row * p.upr;
+  return rg;
+}
+
+// Stage of units [u, un) of the row: element range and aligned interior.
+template <int DT>
+__device__ __forceinline__ Stage stage_of(const RowGeom& rg, int V, int64_t u, int64_t un) {
+  Stage st;
+  st.e0 = (int)((u - rg.ur) * kUnitA);
+  st.e1 = (int)min((int64_t)V, (un - rg.ur) * kUnitA);
+  st.b0 = (uintptr_t)(rg.rp + (int64_t)st.e0 * Elem<DT>::kSize);
+  const uintptr_t b1 = (uintptr_t)(rg.rp + (int64_t)st.e1 * Elem<DT>::kSize);
   st.a0 = (st.b0 + 15) & ~(uintptr_t)15;
   st.a1 = b1 & ~(uintptr_t)15;
   if (st.a1 <= st.a0) st.a0 = st.a1 = st.b0;  // no aligned interior: all scalar
@@ -120,45 +129,123 @@ struct Acc {
   }
 };
 
-template <int DT, int TOPK>
-__device__ __forceinline__ void consume_vec(Acc<TOPK>& a, const uint4 raw, int idx0, float c,
-                                            bool top) {
-  constexpr int VEC = Elem<DT>::kVec;
-  float x[VEC];
-  Elem<DT>::unpack(raw, x);
-  float vm = x[0];
+// Softmax accumulator of one consumer thread: running maximum m, its scaled
+// offset mc = fl(m*c) and the compensated sum (hi, lo) of 2^(z*c - mc).
+struct SAcc {
+  float m, mc, hi, lo;
+  __device__ __forceinline__ void reset() {
+    m = kNegInf;
+    mc = kNegInf;
+    hi = 0.f;
+    lo = 0.f;
+  }
+  __device__ __forceinline__ void raise_max(float vm, float c) {
+    const float mcn = __fmul_rn(vm, c);
+    if (m != kNegInf) pair_scale(hi, lo, exp2f(mc - mcn));
+    m = vm;
+    mc = mcn;
+  }
+  __device__ __forceinline__ void add(float v) {
+    const float y = v - lo;
+    const float t = hi + y;
+    lo = (t - hi) - y;
+    hi = t;
+  }
+  // n logits (all finite, or -inf padding) whose maximum is vm.
+  template <int N>
+  __device__ __forceinline__ void take(const float* x, float vm, float c) {
+    if (vm > m) raise_max(vm, c);
+    float e[N];
 #pragma unroll
-  for (int k = 1; k < VEC; ++k) vm = fmaxf(vm, x[k]);
-  if (vm > a.m) a.raise_max(vm, c);
-  float e[VEC];
+    for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(x[k], c, -mc));
 #pragma unroll
-  for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(x[k], c, -a.mc));
+    for (int w = N / 2; w > 0; w >>= 1)
 #pragma unroll
-  for (int w = VEC / 2; w > 0; w >>= 1)
+      for (int k = 0; k < w; ++k) e[k] += e[k + w];
+    if (N % 2 == 1 && N > 1) e[0] += e[N - 1];
+    add(e[0]);
+  }
+};
+
+// One warp-wide top list: lane l < TOPK holds the l-th best candidate by
+// (logit desc, index asc); (cv, ci) is the TOPK-th entry, known to all lanes.
+// Candidates are offered by ballot and inserted cooperatively, so a lane's
+// rare candidate costs the warp a handful of shuffles instead of a predicated
+// per-thread insertion.
+template <int TOPK>
+struct WarpList {
+  float lv, cv;
+  int li, ci;
+  __device__ __forceinline__ void reset() {
+    lv = cv = kNegInf;
+    li = ci = 0x7fffffff;
+  }
+  // -inf marks padding (empty lanes, partial vectors): never a candidate.
+  __device__ __forceinline__ bool qualifies(float x, int i, float ccut) const {
+    return x != kNegInf && cand_before(x, i, cv, ci) && x >= ccut;
+  }
+  __device__ __forceinline__ void insert(float v, int i) {
+    const int lane = threadIdx.x & 31;
+    const bool before = lane < TOPK && cand_before(lv, li, v, i);
+    const int pos = __popc(__ballot_sync(0xffffffffu, before));
+    if (pos >= TOPK) return;  // warp-uniform
+    const float upv = __shfl_up_sync(0xffffffffu, lv, 1);
+    const int upi = __shfl_up_sync(0xffffffffu, li, 1);
+    if (lane > pos && lane < TOPK) {
+      lv = upv;
+      li = upi;
+    } else if (lane == pos) {
+      lv = v;
+      li = i;
+    }
+    cv = __shfl_sync(0xffffffffu, lv, TOPK - 1);
+    ci = __shfl_sync(0xffffffffu, li, TOPK - 1);
+  }
+  // A lower bound on the TOPK-th largest logit of a block: the TOPK-th
+  // largest of the 32 lane maxima (at least TOPK logits of the block reach
+  // it).  Used while the list is still empty, so that the first block does not
+  // flood it with candidates.
+  __device__ __forceinline__ float boot_bound(float vm) const {
+    const int lane = threadIdx.x & 31;
+    int rank = 0;
 #pragma unroll
-    for (int k = 0; k < w; ++k) e[k] += e[k + w];
-  a.add(e[0]);
-  if constexpr (TOPK > 0) {
-    if (top && vm > a.tv[TOPK - 1]) {
+    for (int j = 0; j < 32; ++j) {
+      const float o = __shfl_sync(0xffffffffu, vm, j);
+      rank += (o > vm || (o == vm && j < lane)) ? 1 : 0;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, rank == TOPK - 1);
+    return __shfl_sync(0xffffffffu, vm, __ffs(m) - 1);
+  }
+  // Offer this lane's N logits x[k] with indices idx0 + (k / VEC) * kstride
+  // + k % VEC; vm is their maximum.  Called by all 32 lanes.  Candidates are
+  // located vector by vector (one vote per vector), then element by element.
+  template <int N, int VEC>
+  __device__ __forceinline__ void offer(const float* x, float vm, int idx0, int kstride,
+                                        float ccut) {
+    if (cv == kNegInf && N * 32 >= TOPK) ccut = fmaxf(ccut, boot_bound(vm));
+    const bool anyq = vm != kNegInf && vm >= cv && vm >= ccut;
+    if (!__any_sync(0xffffffffu, anyq)) return;
 #pragma unroll
-      for (int k = 0; k < VEC; ++k)
-        if (x[k] > a.tv[TOPK - 1]) topk_insert<TOPK>(a.tv, a.ti, x[k], idx0 + k);
+    for (int q = 0; q < N / VEC; ++q) {
+      float qm = x[q * VEC];
+#pragma unroll
+      for (int k = 1; k < VEC; ++k) qm = fmaxf(qm, x[q * VEC + k]);
+      if (!__any_sync(0xffffffffu, anyq && qm != kNegInf && qm >= cv && qm >= ccut)) continue;
+#pragma unroll
+      for (int k = q * VEC; k < (q + 1) * VEC; ++k) {
+        const int ik = idx0 + (k / VEC) * kstride + (k % VEC);
+        unsigned m = __ballot_sync(0xffffffffu, anyq && qualifies(x[k], ik, ccut));
+        while (m) {
+          const int L = __ffs(m) - 1;
+          const float v = __shfl_sync(0xffffffffu, x[k], L);
+          const int i = __shfl_sync(0xffffffffu, ik, L);
+          insert(v, i);
+          m &= m - 1;
+        }
+      }
     }
   }
-}
-
-// Unaligned head/tail elements of a stage.  Head elements precede the stage's
-// vectors in vocabulary order but are folded in after them, so candidates are
-// inserted with the full (logit desc, index asc) order.
-template <int TOPK>
-__device__ __forceinline__ void consume_one(Acc<TOPK>& a, float x, int idx, float c, bool top) {
-  if (x > a.m) a.raise_max(x, c);
-  a.add(ex2(fmaf(x, c, -a.mc)));
-  if constexpr (TOPK > 0) {
-    if (top && cand_before(x, idx, a.tv[TOPK - 1], a.ti[TOPK - 1]))
-      topk_insert_ordered<TOPK>(a.tv, a.ti, x, idx);
-  }
-}
+};
 
 // Fold one stored partial into a lane's accumulator (row merges).
 template <int TOPK>
@@ -369,14 +456,44 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
   }
 }
 
+// Warp roles: warps 0..kConsumerWarps-1 reduce staged data, warp
+// kConsumerWarps issues the bulk copies, warp kConsumerWarps+1 merges each row
+// piece's per-warp results and does all global-memory epilogue work, so the
+// consumer warps never wait for it.  Piece results pass through a queue of
+// kPieceSlots shared-memory slots guarded by mbarriers.
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;
+constexpr int kStreamThreads = (kConsumerWarps + 2) * 32;
+constexpr int kPieceSlots = 4;
+
+// The row pieces of one CTA, in order: [u, ure) units of row `row`.
+struct PieceIter {
+  int64_t u, u_end, upr;
+  __device__ __forceinline__ bool next(int64_t& row, int64_t& pu0, int64_t& pu1) {
+    if (u >= u_end) return false;
+    row = u / upr;
+    pu0 = u;
+    pu1 = min((row + 1) * upr, u_end);
+    u = pu1;
+    return true;
+  }
+};
+
 template <int DT, int TOPK>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamParams p) {
+__global__ void __launch_bounds__(kStreamThreads, 1)
+    stream_kernel(const __grid_constant__ StreamParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesA * kStageBytes);
   uint64_t* empty = full + kStagesA;
-  PieceRed<TOPK>* red = reinterpret_cast<PieceRed<TOPK>*>(empty + kStagesA);  // [2]
+  uint64_t* pfull = empty + kStagesA;
+  uint64_t* pempty = pfull + kPieceSlots;
+  PieceRed<TOPK>* slots = reinterpret_cast<PieceRed<TOPK>*>(pempty + kPieceSlots);
   __shared__ int s_err;
+  // Top-list pruning bound shared by the CTA's warps: (row << 32) | ordered
+  // float.  Rows only increase within a CTA, so a value of another row is
+  // never mistaken for the current row's.
+  __shared__ unsigned long long s_cut;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -391,25 +508,31 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       mbar_init(full + i, 1);
       mbar_init(empty + i, kConsumerWarps);
     }
+    for (int i = 0; i < kPieceSlots; ++i) {
+      mbar_init(pfull + i, kConsumerWarps);
+      mbar_init(pempty + i, 1);
+    }
     s_err = 0;
+    s_cut = 0ull;
     fence_barrier_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ---------------- producer ----------------
     if (lane == 0) {
       int n = 0;
-      for (int64_t u = u_begin; u < u_end;) {
-        const int64_t row = u / p.upr;
-        const int64_t ure = min((row + 1) * p.upr, u_end);
-        for (int64_t un = 0; u < ure; u = un) {
-          un = min(u + ups, ure);
-          const Stage st = stage_geometry<DT>(p, row, u, un);
+      PieceIter it{u_begin, u_end, p.upr};
+      int64_t row, pu0, pu1;
+      while (it.next(row, pu0, pu1)) {
+        const RowGeom rg = row_geom<DT>(p, row);
+        for (int64_t u = pu0, un = 0; u < pu1; u = un) {
+          un = min(u + ups, pu1);
+          const Stage st = stage_of<DT>(rg, p.V, u, un);
           const int slot = n % kStagesA;
           if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
           const uint32_t bytes = (uint32_t)(st.a1 - st.a0);
-          const bool tsrc = (row % p.rpg) < p.nt;
+          const bool tsrc = rg.is_t;
           if (bytes > 0 && !s_err &&
               SSD_CHK(in_range(st.a0, st.a1, tsrc ? p.t_lo : p.d_lo, tsrc ? p.t_hi : p.d_hi),
                       p.dbg, 1, st.a0, st.a1)) {
@@ -429,132 +552,205 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     return;
   }
 
-  // ---------------- consumers ----------------
   const float c = p.c;
-  Acc<TOPK> a;
+  if (warp == kEpilogueWarp) {
+    // ---------------- epilogue: merge, publish, finalise ----------------
+    PieceIter it{u_begin, u_end, p.upr};
+    int64_t row, pu0, pu1;
+    for (int piece = 0; it.next(row, pu0, pu1); ++piece) {
+      const int slot = piece % kPieceSlots;
+      mbar_wait(pfull + slot, (piece / kPieceSlots) & 1, &s_err, p.status);
+      const PieceRed<TOPK>& R = slots[slot];
+      const int64_t g = row / p.rpg;
+      const int jr = (int)(row - g * p.rpg);
+      const bool is_t = jr < p.nt;
+      const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
+      Acc<TOPK> b;
+      b.reset();
+      if (lane < kConsumerWarps) {
+        b.m = R.m[lane];
+        b.mc = b.m == kNegInf ? kNegInf : __fmul_rn(b.m, c);
+        b.hi = R.hi[lane];
+        b.lo = R.lo[lane];
+        if (TOPK > 0 && top) {
+#pragma unroll
+          for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
+            b.tv[k] = R.tv[lane][k];
+            b.ti[k] = R.ti[lane][k];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pempty + slot);  // the slot may be refilled
+      float M, MC, Shi, Slo;
+      warp_softmax_merge(b.m, b.mc, b.hi, b.lo, c, M, MC, Shi, Slo);
+      if constexpr (TOPK > 0) {
+        if (top) warp_topk_merge<TOPK>(b.tv, b.ti);
+      }
+      const int64_t r0u = row * p.upr;
+      const int64_t c_lo = r0u / p.upc;
+      const int64_t c_hi = (r0u + p.upr - 1) / p.upc;
+      if (c_lo == c_hi) {
+        finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, b, top);
+        continue;
+      }
+      // row shared with other CTAs: publish the partial, last arrival merges
+      if (!SSD_CHK(row + blockIdx.x < p.NR + kMaxGrid && row < p.NR, p.dbg, 6, row, blockIdx.x))
+        continue;
+      RowPartial* slotp = p.partials + (row + blockIdx.x);
+      if (lane == 0) {
+        slotp->m = M;
+        slotp->s_hi = Shi;
+        slotp->s_lo = Slo;
+#pragma unroll
+        for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
+          slotp->tv[k] = (TOPK > 0 && top) ? b.tv[k] : kNegInf;
+          slotp->ti[k] = (TOPK > 0 && top) ? b.ti[k] : 0x7fffffff;
+        }
+      }
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(p.row_cnt + row, 1) == (int)(c_hi - c_lo);
+        if (last) __threadfence();
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      Acc<TOPK> mrg;
+      mrg.reset();
+      for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32)
+        fold_partial<TOPK>(mrg, p.partials + (row + cc), c, top);
+      warp_softmax_merge(mrg.m, mrg.mc, mrg.hi, mrg.lo, c, M, MC, Shi, Slo);
+      if constexpr (TOPK > 0) {
+        if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti);
+      }
+      finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, mrg, top);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  SAcc a;
+  WarpList<(TOPK > 0 ? TOPK : 1)> wl;
+  constexpr int VEC = Elem<DT>::kVec;
   int n = 0;
-  int piece = 0;
-  for (int64_t u = u_begin; u < u_end; ++piece) {
-    const int64_t row = u / p.upr;
-    const int64_t ure = min((row + 1) * p.upr, u_end);
+  PieceIter it{u_begin, u_end, p.upr};
+  int64_t row, pu0, pu1;
+  for (int piece = 0; it.next(row, pu0, pu1); ++piece) {
     const int64_t g = row / p.rpg;
     const int jr = (int)(row - g * p.rpg);
     const bool is_t = jr < p.nt;
     const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
+    const RowGeom rg = row_geom<DT>(p, row);
     a.reset();
-    for (int64_t un = 0; u < ure; u = un) {
-      un = min(u + ups, ure);
-      const Stage st = stage_geometry<DT>(p, row, u, un);
+    wl.reset();
+    float ccut = kNegInf;       // CTA-wide pruning bound for this row's top list
+    float published = kNegInf;  // this warp's last published cut
+    for (int64_t u = pu0, un = 0; u < pu1; u = un) {
+      un = min(u + ups, pu1);
+      const Stage st = stage_of<DT>(rg, p.V, u, un);
       const int slot = n % kStagesA;
       mbar_wait(full + slot, (n / kStagesA) & 1, &s_err, p.status);
       const int nvec = (int)((st.a1 - st.a0) >> 4);
       const int ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
       const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
-#pragma unroll 4
-      for (int v = tid; v < nvec; v += kConsumers)
-        if (SSD_CHK(v < kStageBytes / 16, p.dbg, 10, v, nvec))
-          consume_vec<DT, TOPK>(a, sv[v], ei0 + v * Elem<DT>::kVec, c, top);
-      // unaligned head / tail elements straight from global memory
+      constexpr int kVecs = kStageBytes / 16;
+      constexpr int kVpt = kVecs / kConsumers;
+      if (nvec == kVecs) {
+        // full stage: this thread's kVpt vectors, loaded first
+        uint4 raw[kVpt];
+#pragma unroll
+        for (int k = 0; k < kVpt; ++k) raw[k] = sv[tid + k * kConsumers];
+        constexpr int N = kVpt * VEC;
+        float x[N];
+#pragma unroll
+        for (int k = 0; k < kVpt; ++k) Elem<DT>::unpack(raw[k], x + k * VEC);
+        float vm = fmaxf(x[0], x[1]);
+#pragma unroll
+        for (int k = 2; k < N; k += 2) vm = fmax3(vm, x[k], x[k + 1]);
+        a.take<N>(x, vm, c);
+        if (TOPK > 0 && top)
+          wl.template offer<N, VEC>(x, vm, ei0 + tid * VEC, kConsumers * VEC, ccut);
+      } else {
+        // partial stage: warp-strided vectors so that every lane takes part
+        for (int v0 = warp * 32; v0 < nvec; v0 += kConsumers) {
+          const int v = v0 + lane;
+          float x[VEC];
+          float vm = kNegInf;
+          if (v < nvec && SSD_CHK(v < kVecs, p.dbg, 10, v, nvec)) {
+            Elem<DT>::unpack(sv[v], x);
+            vm = x[0];
+#pragma unroll
+            for (int k = 1; k < VEC; ++k) vm = fmaxf(vm, x[k]);
+            a.take<VEC>(x, vm, c);
+          } else {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) x[k] = kNegInf;
+          }
+          if (TOPK > 0 && top) wl.template offer<VEC, VEC>(x, vm, ei0 + v * VEC, 0, ccut);
+        }
+      }
+      // unaligned head / tail elements (fewer than 32) by warp 0, from global memory
       const int hc = nvec > 0 ? (int)((st.a0 - st.b0) / Elem<DT>::kSize) : st.e1 - st.e0;
-      const int ei1 = ei0 + nvec * Elem<DT>::kVec;
+      const int ei1 = ei0 + nvec * VEC;
       const int tc = nvec > 0 ? st.e1 - ei1 : 0;
-      for (int f = tid; f < hc + tc; f += kConsumers) {
-        const int idx = f < hc ? st.e0 + f : ei1 + (f - hc);
-        const uintptr_t fa = st.b0 + (uintptr_t)(idx - st.e0) * Elem<DT>::kSize;
-        const bool tsrc = is_t;
-        if (!SSD_CHK(in_range(fa, fa + Elem<DT>::kSize, tsrc ? p.t_lo : p.d_lo,
-                              tsrc ? p.t_hi : p.d_hi), p.dbg, 2, idx, st.e0))
-          continue;
-        const float x = Elem<DT>::load(reinterpret_cast<const void*>(st.b0),
-                                       (int64_t)(idx - st.e0));
-        consume_one<TOPK>(a, x, idx, c, top);
+      if (warp == 0) {
+        for (int f0 = 0; f0 < hc + tc; f0 += 32) {
+          const int f = f0 + lane;
+          float x = kNegInf;
+          int idx = 0;
+          if (f < hc + tc) {
+            idx = f < hc ? st.e0 + f : ei1 + (f - hc);
+            const uintptr_t fa = st.b0 + (uintptr_t)(idx - st.e0) * Elem<DT>::kSize;
+            if (SSD_CHK(in_range(fa, fa + Elem<DT>::kSize, is_t ? p.t_lo : p.d_lo,
+                                 is_t ? p.t_hi : p.d_hi), p.dbg, 2, idx, st.e0)) {
+              x = Elem<DT>::load(reinterpret_cast<const void*>(st.b0), (int64_t)(idx - st.e0));
+              a.take<1>(&x, x, c);
+            }
+          }
+          if (TOPK > 0 && top) wl.template offer<1, 1>(&x, x, idx, 0, ccut);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + slot);
       ++n;
+      if (TOPK > 0 && top) {
+        // The warp holds TOPK candidates >= its cut cv, so no logit strictly
+        // below the largest cut of the CTA's warps (for this row) can enter
+        // the row's top list.  A warp publishes its cut only when it rose.
+        const unsigned long long tag = (unsigned long long)(uint32_t)row << 32;
+        unsigned long long w = 0ull;
+        if (lane == 0) {
+          if (wl.cv != kNegInf && wl.cv > published) {
+            atomicMax(&s_cut, tag | ord_float(wl.cv));
+            published = wl.cv;
+          }
+          w = *reinterpret_cast<volatile unsigned long long*>(&s_cut);
+        }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if ((w >> 32) == (uint32_t)row) ccut = fmaxf(ccut, unord_float((uint32_t)w));
+      }
     }
 
-    // ---- piece reduction: warp, then CTA ----
+    // ---- hand the piece's per-warp results to the epilogue warp ----
     float M, MC, Shi, Slo;
     warp_softmax_merge(a.m, a.mc, a.hi, a.lo, c, M, MC, Shi, Slo);
-    if constexpr (TOPK > 0) {
-      if (top) warp_topk_merge<TOPK>(a.tv, a.ti);
-    }
-    PieceRed<TOPK>& R = red[piece & 1];
+    const int ps = piece % kPieceSlots;
+    if (lane == 0 && piece >= kPieceSlots)
+      mbar_wait(pempty + ps, ((piece / kPieceSlots) - 1) & 1, &s_err, p.status);
+    __syncwarp();
+    PieceRed<TOPK>& R = slots[ps];
     if (lane == 0) {
       R.m[warp] = M;
       R.hi[warp] = Shi;
       R.lo[warp] = Slo;
-#pragma unroll
-      for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
-        R.tv[warp][k] = a.tv[k];
-        R.ti[warp][k] = a.ti[k];
-      }
     }
-    consumer_sync();
-    if (warp != 0) continue;
-
-    // warp 0: combine the eight warp results
-    Acc<TOPK> b;
-    b.reset();
-    if (lane < kConsumerWarps) {
-      b.m = R.m[lane];
-      b.mc = b.m == kNegInf ? kNegInf : __fmul_rn(b.m, c);
-      b.hi = R.hi[lane];
-      b.lo = R.lo[lane];
-      if (TOPK > 0 && top) {
-#pragma unroll
-        for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
-          b.tv[k] = R.tv[lane][k];
-          b.ti[k] = R.ti[lane][k];
-        }
-      }
+    if (lane < (TOPK > 0 ? TOPK : 1)) {
+      R.tv[warp][lane] = (TOPK > 0 && top) ? wl.lv : kNegInf;
+      R.ti[warp][lane] = (TOPK > 0 && top) ? wl.li : 0x7fffffff;
     }
-    warp_softmax_merge(b.m, b.mc, b.hi, b.lo, c, M, MC, Shi, Slo);
-    if constexpr (TOPK > 0) {
-      if (top) warp_topk_merge<TOPK>(b.tv, b.ti);
-    }
-
-    const int64_t r0u = row * p.upr;
-    const int64_t c_lo = r0u / p.upc;
-    const int64_t c_hi = (r0u + p.upr - 1) / p.upc;
-    if (c_lo == c_hi) {
-      finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, b, top);
-      continue;
-    }
-    // row shared with other CTAs: publish the partial, last arrival merges
-    if (!SSD_CHK(row + blockIdx.x < p.NR + kMaxGrid && row < p.NR, p.dbg, 6, row, blockIdx.x))
-      continue;
-    RowPartial* slotp = p.partials + (row + blockIdx.x);
-    if (lane == 0) {
-      slotp->m = M;
-      slotp->s_hi = Shi;
-      slotp->s_lo = Slo;
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) {
-        slotp->tv[k] = (TOPK > 0 && top) ? b.tv[k] : kNegInf;
-        slotp->ti[k] = (TOPK > 0 && top) ? b.ti[k] : 0x7fffffff;
-      }
-    }
-    int last = 0;
-    if (lane == 0) {
-      __threadfence();
-      last = atomicAdd(p.row_cnt + row, 1) == (int)(c_hi - c_lo);
-      if (last) __threadfence();
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-    Acc<TOPK> mrg;
-    mrg.reset();
-    for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32)
-      fold_partial<TOPK>(mrg, p.partials + (row + cc), c, top);
-    warp_softmax_merge(mrg.m, mrg.mc, mrg.hi, mrg.lo, c, M, MC, Shi, Slo);
-    if constexpr (TOPK > 0) {
-      if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti);
-    }
-    finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, mrg, top);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pfull + ps);
   }
 }
 
@@ -564,7 +760,7 @@ cudaError_t launch_t(const StreamParams& p, int grid, cudaStream_t s) {
   auto kern = stream_kernel<DT, TOPK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, s>>>(p);
+  kern<<<grid, kStreamThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -583,8 +779,8 @@ cudaError_t launch_dt(const StreamParams& p, int topk, int grid, cudaStream_t s)
 }  // namespace
 
 int stream_smem_bytes() {
-  return kStagesA * kStageBytes + 2 * kStagesA * (int)sizeof(uint64_t) +
-         2 * (int)sizeof(PieceRed<kMaxTopK>);
+  return kStagesA * kStageBytes + 2 * (kStagesA + kPieceSlots) * (int)sizeof(uint64_t) +
+         kPieceSlots * (int)sizeof(PieceRed<kMaxTopK>);
 }
 
 cudaError_t launch_stream(const StreamParams& p, int dtype, int topk, int grid, cudaStream_t s) {
