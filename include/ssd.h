@@ -135,6 +135,39 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ssd_verify_noalloc -- ssd_verify without a caller workspace.  The pages have
+ * no counterpart: this is a deployment convenience.
+ *
+ * For callers that cannot allocate device memory where they call the library
+ * (a plugin of an inference runtime whose enqueue hook may not allocate, a
+ * process whose device memory belongs to a pool allocator, a decode loop that
+ * cannot pay for cudaMalloc and its implicit synchronisation).  The scratch
+ * space is a SSD_NOALLOC_SCRATCH_BYTES array compiled into the library; every
+ * GPU that loads the library holds it until the process exits.  Arguments and
+ * results are those of ssd_verify.
+ *   - Requests whose ssd_verify_workspace_size(B, K, Kq, V) exceeds
+ *     SSD_NOALLOC_SCRATCH_BYTES return SSD_ERR_WORKSPACE (use ssd_verify with
+ *     your own workspace); nothing is enqueued.  4 MiB covers, for example,
+ *     B = 256 sequences with K = 8 at V = 151936.
+ *   - The first call on a device looks up the array's address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - All calls on a device share the array; the parts that must start at
+ *     zero are cleared at the start of each call.  Calls whose work overlaps
+ *     on the GPU (different streams or host threads) race on the array and
+ *     must be serialised by the caller.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ *     routine is called.
+ * ------------------------------------------------------------------------- */
+#define SSD_NOALLOC_SCRATCH_BYTES (4u << 20)
+ssd_status ssd_verify_noalloc(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                              int Kq, int V, float T, const int32_t* draft_tokens,
+                              const uint64_t* seeds, uint32_t round, const int32_t* fanout,
+                              float C, int32_t* accept_len, int32_t* bonus, float* resid_mass,
+                              int32_t* guesses, float* guess_q, int Fmax, int32_t* dev_status,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
  * ssd_topf_bonus -- bonus-token guesses alone.  [SSD-note] §"怎么猜奖励 token":
  * the top-F_j draft logits of position j, excluding the token already sampled
  * there.
