@@ -181,6 +181,18 @@ struct Elem<1> {  // fp32
   }
 };
 
+// Element k (runtime index) of a 16-byte vector, without spilling the vector.
+template <int DT>
+__device__ __forceinline__ float vec_elem(const uint4 v, int k) {
+  if constexpr (DT == 0) {
+    const uint32_t w = (k < 4) ? ((k < 2) ? v.x : v.y) : ((k < 6) ? v.z : v.w);
+    return __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  } else {
+    const uint32_t w = (k < 2) ? ((k == 0) ? v.x : v.y) : ((k == 2) ? v.z : v.w);
+    return __uint_as_float(w);
+  }
+}
+
 __device__ __forceinline__ const char* row_ptr(const void* base, int64_t row, int64_t stride,
                                                int esize) {
   return reinterpret_cast<const char*>(base) + row * stride * esize;

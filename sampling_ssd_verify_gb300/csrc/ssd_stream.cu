@@ -176,9 +176,11 @@ template <int TOPK>
 struct WarpList {
   float lv, cv;
   int li, ci;
-  __device__ __forceinline__ void reset() {
+  int R;  // entries the row needs (F_j + 1 <= TOPK); the cut is entry R - 1
+  __device__ __forceinline__ void reset(int need) {
     lv = cv = kNegInf;
     li = ci = 0x7fffffff;
+    R = need;
   }
   // -inf marks padding (empty lanes, partial vectors): never a candidate.
   __device__ __forceinline__ bool qualifies(float x, int i, float ccut) const {
@@ -186,20 +188,20 @@ struct WarpList {
   }
   __device__ __forceinline__ void insert(float v, int i) {
     const int lane = threadIdx.x & 31;
-    const bool before = lane < TOPK && cand_before(lv, li, v, i);
+    const bool before = lane < R && cand_before(lv, li, v, i);
     const int pos = __popc(__ballot_sync(0xffffffffu, before));
-    if (pos >= TOPK) return;  // warp-uniform
+    if (pos >= R) return;  // warp-uniform
     const float upv = __shfl_up_sync(0xffffffffu, lv, 1);
     const int upi = __shfl_up_sync(0xffffffffu, li, 1);
-    if (lane > pos && lane < TOPK) {
+    if (lane > pos && lane < R) {
       lv = upv;
       li = upi;
     } else if (lane == pos) {
       lv = v;
       li = i;
     }
-    cv = __shfl_sync(0xffffffffu, lv, TOPK - 1);
-    ci = __shfl_sync(0xffffffffu, li, TOPK - 1);
+    cv = __shfl_sync(0xffffffffu, lv, R - 1);
+    ci = __shfl_sync(0xffffffffu, li, R - 1);
   }
   // A lower bound on the TOPK-th largest logit of a block: the TOPK-th
   // largest of the 32 lane maxima (at least TOPK logits of the block reach
@@ -213,31 +215,35 @@ struct WarpList {
       const float o = __shfl_sync(0xffffffffu, vm, j);
       rank += (o > vm || (o == vm && j < lane)) ? 1 : 0;
     }
-    const unsigned m = __ballot_sync(0xffffffffu, rank == TOPK - 1);
+    const unsigned m = __ballot_sync(0xffffffffu, rank == R - 1);
     return __shfl_sync(0xffffffffu, vm, __ffs(m) - 1);
   }
-  // Offer this lane's N logits x[k] with indices idx0 + (k / VEC) * kstride
-  // + k % VEC; vm is their maximum.  Called by all 32 lanes.  Candidates are
-  // located vector by vector (one vote per vector), then element by element.
-  template <int N, int VEC>
-  __device__ __forceinline__ void offer(const float* x, float vm, int idx0, int kstride,
-                                        float ccut) {
-    if (cv == kNegInf && N * 32 >= TOPK) ccut = fmaxf(ccut, boot_bound(vm));
-    const bool anyq = vm != kNegInf && vm >= cv && vm >= ccut;
-    if (!__any_sync(0xffffffffu, anyq)) return;
+  // Offer the lane's logits held as NV raw 16-byte vectors raw[q] (element k
+  // of vector q has index idx0 + q * kstride + k; vm is the maximum over all
+  // of them, vq[q] the maximum of vector q; padding is -inf).  Called by all
+  // 32 lanes.  The common case -- no lane holds a candidate -- costs one vote.
+  template <int DT, int NV>
+  __device__ __forceinline__ void offer(const uint4* raw, const float* vq, float vm, int idx0,
+                                        int kstride, float ccut);
+  // The rare path: locate candidates vector by vector (one vote each), then
+  // element by element with a runtime index.
+  template <int DT, int NV>
+  __device__ __forceinline__ void offer_rare(const uint4* raw, const float* vq, int idx0,
+                                             int kstride, float ccut, bool anyq) {
+    constexpr int VEC = Elem<DT>::kVec;
 #pragma unroll
-    for (int q = 0; q < N / VEC; ++q) {
-      float qm = x[q * VEC];
-#pragma unroll
-      for (int k = 1; k < VEC; ++k) qm = fmaxf(qm, x[q * VEC + k]);
-      if (!__any_sync(0xffffffffu, anyq && qm != kNegInf && qm >= cv && qm >= ccut)) continue;
-#pragma unroll
-      for (int k = q * VEC; k < (q + 1) * VEC; ++k) {
-        const int ik = idx0 + (k / VEC) * kstride + (k % VEC);
-        unsigned m = __ballot_sync(0xffffffffu, anyq && qualifies(x[k], ik, ccut));
+    for (int q = 0; q < NV; ++q) {
+      const uint4 rq = raw[q];
+      const float mq = vq[q];
+      if (!__any_sync(0xffffffffu, anyq && mq != kNegInf && mq >= cv && mq >= ccut)) continue;
+#pragma unroll 1
+      for (int k = 0; k < VEC; ++k) {
+        const float xk = vec_elem<DT>(rq, k);
+        const int ik = idx0 + q * kstride + k;
+        unsigned m = __ballot_sync(0xffffffffu, anyq && mq != kNegInf && qualifies(xk, ik, ccut));
         while (m) {
           const int L = __ffs(m) - 1;
-          const float v = __shfl_sync(0xffffffffu, x[k], L);
+          const float v = __shfl_sync(0xffffffffu, xk, L);
           const int i = __shfl_sync(0xffffffffu, ik, L);
           insert(v, i);
           m &= m - 1;
@@ -245,7 +251,27 @@ struct WarpList {
       }
     }
   }
+  // One logit per lane (unaligned stage fragments); -inf is padding.
+  __device__ __forceinline__ void offer1(float x, int idx, float ccut) {
+    unsigned m = __ballot_sync(0xffffffffu, qualifies(x, idx, ccut));
+    while (m) {
+      const int L = __ffs(m) - 1;
+      insert(__shfl_sync(0xffffffffu, x, L), __shfl_sync(0xffffffffu, idx, L));
+      m &= m - 1;
+    }
+  }
 };
+
+template <int TOPK>
+template <int DT, int NV>
+__device__ __forceinline__ void WarpList<TOPK>::offer(const uint4* raw, const float* vq, float vm,
+                                                      int idx0, int kstride, float ccut) {
+  constexpr int VEC = Elem<DT>::kVec;
+  if (cv == kNegInf && NV * VEC * 32 >= R) ccut = fmaxf(ccut, boot_bound(vm));
+  const bool anyq = vm != kNegInf && vm >= cv && vm >= ccut;
+  if (!__any_sync(0xffffffffu, anyq)) return;
+  offer_rare<DT, NV>(raw, vq, idx0, kstride, ccut, anyq);
+}
 
 // Fold one stored partial into a lane's accumulator (row merges).
 template <int TOPK>
@@ -643,7 +669,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
     const RowGeom rg = row_geom<DT>(p, row);
     a.reset();
-    wl.reset();
+    wl.reset(top ? p.F[jr - p.nt] + 1 : 1);
     float ccut = kNegInf;       // CTA-wide pruning bound for this row's top list
     float published = kNegInf;  // this warp's last published cut
     for (int64_t u = pu0, un = 0; u < pu1; u = un) {
@@ -665,29 +691,37 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         float x[N];
 #pragma unroll
         for (int k = 0; k < kVpt; ++k) Elem<DT>::unpack(raw[k], x + k * VEC);
-        float vm = fmaxf(x[0], x[1]);
+        float vq[kVpt];
 #pragma unroll
-        for (int k = 2; k < N; k += 2) vm = fmax3(vm, x[k], x[k + 1]);
+        for (int q = 0; q < kVpt; ++q) {
+          float t = fmaxf(x[q * VEC], x[q * VEC + 1]);
+#pragma unroll
+          for (int k = 2; k < VEC; k += 2) t = fmax3(t, x[q * VEC + k], x[q * VEC + k + 1]);
+          vq[q] = t;
+        }
+        float vm = vq[0];
+#pragma unroll
+        for (int q = 1; q < kVpt; ++q) vm = fmaxf(vm, vq[q]);
         a.take<N>(x, vm, c);
         if (TOPK > 0 && top)
-          wl.template offer<N, VEC>(x, vm, ei0 + tid * VEC, kConsumers * VEC, ccut);
+          wl.template offer<DT, kVpt>(raw, vq, vm, ei0 + tid * VEC, kConsumers * VEC, ccut);
       } else {
         // partial stage: warp-strided vectors so that every lane takes part
         for (int v0 = warp * 32; v0 < nvec; v0 += kConsumers) {
           const int v = v0 + lane;
           float x[VEC];
           float vm = kNegInf;
+          uint4 rv = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+          if (DT == 1) rv = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
           if (v < nvec && SSD_CHK(v < kVecs, p.dbg, 10, v, nvec)) {
-            Elem<DT>::unpack(sv[v], x);
+            rv = sv[v];
+            Elem<DT>::unpack(rv, x);
             vm = x[0];
 #pragma unroll
             for (int k = 1; k < VEC; ++k) vm = fmaxf(vm, x[k]);
             a.take<VEC>(x, vm, c);
-          } else {
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) x[k] = kNegInf;
           }
-          if (TOPK > 0 && top) wl.template offer<VEC, VEC>(x, vm, ei0 + v * VEC, 0, ccut);
+          if (TOPK > 0 && top) wl.template offer<DT, 1>(&rv, &vm, vm, ei0 + v * VEC, 0, ccut);
         }
       }
       // unaligned head / tail elements (fewer than 32) by warp 0, from global memory
@@ -708,7 +742,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
               a.take<1>(&x, x, c);
             }
           }
-          if (TOPK > 0 && top) wl.template offer<1, 1>(&x, x, idx, 0, ccut);
+          if (TOPK > 0 && top) wl.offer1(x, idx, ccut);
         }
       }
       __syncwarp();
