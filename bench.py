@@ -21,6 +21,7 @@ workload on the host cores.  Under torchrun each rank runs its own batch
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -154,6 +155,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     ssd.build()
     w = WORKLOADS[args.workload]
+    if args.batch or args.vocab:
+        w = dataclasses.replace(w, B=args.batch or w.B, V=args.vocab or w.V,
+                                name=f"{w.name} [B={args.batch or w.B}, V={args.vocab or w.V}]")
     B, K, Kq, V = w.B, w.K, w.Kq, w.V
     F = np.asarray(w.fanout, dtype=np.int32)
     bt = make_batch(w, seed=w.seed + 7919 * rank)
@@ -394,6 +398,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c5", choices=["c2", "c3", "c4", "c5"])
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch B")
+    ap.add_argument("--vocab", type=int, default=0, help="override the workload's vocabulary V")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

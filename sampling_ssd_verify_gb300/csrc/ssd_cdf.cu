@@ -52,14 +52,43 @@ __device__ __forceinline__ float fetch(const Half& h, int y, const CdfParams& p,
 }
 
 // The draw weight of token y given its target logit zt and draft logit zd.
+// The three kinds of draw, as separate formulas so that unit loops can be
+// specialised; weight() dispatches.  kind_of() classifies a group.
+enum DrawKind : int { kResidual = 0, kTarget = 1, kSaguaro = 2 };
+
+__device__ __forceinline__ int kind_of(const GroupParams& gp) {
+  return gp.use_d ? (gp.sign_d > 0 ? kSaguaro : kResidual) : kTarget;
+}
+
+template <bool HAS_S>
+__device__ __forceinline__ float q_scale(const GroupParams& gp, int y, float zd) {
+  if (!HAS_S) return gp.scale_out;
+  const bool inS = zd > gp.theta || (zd == gp.theta && y <= gp.itheta);
+  return inS ? gp.scale_in : gp.scale_out;
+}
+
+template <int KIND, bool HAS_S>
+__device__ __forceinline__ float weight_k(const GroupParams& gp, float c, int y, float zt,
+                                          float zd) {
+  if (KIND == kTarget) return ex2(fmaf(zt, c, -gp.mc_t)) * gp.inv_st;
+  const float q = ex2(fmaf(zd, c, -gp.mc_d)) * q_scale<HAS_S>(gp, y, zd);
+  if (KIND == kSaguaro) return q;
+  const float pt = ex2(fmaf(zt, c, -gp.mc_t)) * gp.inv_st;
+  return fmaxf(pt - q, 0.f);
+}
+
 __device__ __forceinline__ float weight(const GroupParams& gp, float c, int y, float zt,
                                         float zd) {
-  float p = 0.f;
-  if (gp.use_t) p = ex2(fmaf(zt, c, -gp.mc_t)) * gp.inv_st;
-  if (!gp.use_d) return p;
-  const bool inS = zd > gp.theta || (zd == gp.theta && y <= gp.itheta);
-  const float q = ex2(fmaf(zd, c, -gp.mc_d)) * (inS ? gp.scale_in : gp.scale_out);
-  return gp.sign_d > 0 ? q : fmaxf(p - q, 0.f);
+  const bool has_s = gp.theta != INFINITY;
+  switch (kind_of(gp)) {
+    case kTarget: return weight_k<kTarget, false>(gp, c, y, zt, zd);
+    case kSaguaro:
+      return has_s ? weight_k<kSaguaro, true>(gp, c, y, zt, zd)
+                   : weight_k<kSaguaro, false>(gp, c, y, zt, zd);
+    default:
+      return has_s ? weight_k<kResidual, true>(gp, c, y, zt, zd)
+                   : weight_k<kResidual, false>(gp, c, y, zt, zd);
+  }
 }
 
 template <int DT>
@@ -345,28 +374,52 @@ struct CdfRing {
 };
 
 // Sum of the draw weights of one whole unit whose elements sit 16-byte
-// aligned in shared memory (vectorised fast path of one warp).
-template <int DT>
-__device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupParams& gp,
-                                               const Half& ht, const Half& hd, int ue0) {
+// aligned in shared memory (vectorised fast path of one warp), specialised
+// per kind of draw.
+template <int DT, int KIND, bool HAS_S>
+__device__ __forceinline__ float unit_sum_k(const CdfParams& p, const GroupParams& gp,
+                                            const Half& ht, const Half& hd, int ue0) {
   constexpr int VEC = Elem<DT>::kVec;
   constexpr int NV = kUnitB / VEC / 32;
   const int lane = threadIdx.x & 31;
   const uint4* st4 = reinterpret_cast<const uint4*>(ht.sm + (ue0 - ht.ei0) * Elem<DT>::kSize);
   const uint4* sd4 = reinterpret_cast<const uint4*>(hd.sm + (ue0 - hd.ei0) * Elem<DT>::kSize);
+  uint4 rt[NV], rd[NV];
+#pragma unroll
+  for (int m = 0; m < NV; ++m) {
+    if (KIND != kSaguaro) rt[m] = st4[lane + 32 * m];
+    if (KIND != kTarget) rd[m] = sd4[lane + 32 * m];
+  }
   float s = 0.f;
 #pragma unroll
   for (int m = 0; m < NV; ++m) {
     const int vi = lane + 32 * m;
     float zt[VEC], zd[VEC];
+    if (KIND != kSaguaro) Elem<DT>::unpack(rt[m], zt);
+    if (KIND != kTarget) Elem<DT>::unpack(rd[m], zd);
+    float sv = 0.f;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) zt[e] = zd[e] = 0.f;
-    if (gp.use_t) Elem<DT>::unpack(st4[vi], zt);
-    if (gp.use_d) Elem<DT>::unpack(sd4[vi], zd);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) s += weight(gp, p.c, ue0 + vi * VEC + e, zt[e], zd[e]);
+    for (int e = 0; e < VEC; ++e)
+      sv += weight_k<KIND, HAS_S>(gp, p.c, ue0 + vi * VEC + e, KIND != kSaguaro ? zt[e] : 0.f,
+                                  KIND != kTarget ? zd[e] : 0.f);
+    s += sv;
   }
   return s;
+}
+
+template <int DT>
+__device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupParams& gp,
+                                               const Half& ht, const Half& hd, int ue0) {
+  const bool has_s = gp.theta != INFINITY;
+  switch (kind_of(gp)) {
+    case kTarget: return unit_sum_k<DT, kTarget, false>(p, gp, ht, hd, ue0);
+    case kSaguaro:
+      return has_s ? unit_sum_k<DT, kSaguaro, true>(p, gp, ht, hd, ue0)
+                   : unit_sum_k<DT, kSaguaro, false>(p, gp, ht, hd, ue0);
+    default:
+      return has_s ? unit_sum_k<DT, kResidual, true>(p, gp, ht, hd, ue0)
+                   : unit_sum_k<DT, kResidual, false>(p, gp, ht, hd, ue0);
+  }
 }
 
 template <int DT>
