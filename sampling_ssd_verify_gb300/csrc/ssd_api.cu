@@ -101,6 +101,8 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.c = (float)(1.4426950408889634 / (double)T);  // log2(e) / T
   p.row_cnt = cnt;
   p.grp_cnt = cnt + L.NR;
+  p.row_cut = reinterpret_cast<uint32_t*>(cnt + L.NR + 2 * groups);
+  p.chunk_ctr = reinterpret_cast<unsigned long long*>(ws + L.cnt_off + L.ctr_off);
   p.partials = reinterpret_cast<RowPartial*>(ws + L.part_off);
   p.rowres = reinterpret_cast<RowResult*>(ws + L.rowres_off);
   p.gparams = reinterpret_cast<GroupParams*>(ws + L.gp_off);
@@ -141,9 +143,24 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   return SSD_OK;
 }
 
+// Chunks of the streaming pass.  CTAs take chunks from a global counter, so
+// a CTA that meets costlier rows (more top-list insertions) takes fewer.
+// Whole rows when there are at least two per CTA (a row split over CTAs
+// costs a partial merge and restarts its top-list pruning); otherwise rows
+// are cut into up to kMaxChunks equal chunks, about four per CTA in all.
 ssd_status run_stream(StreamParams& p, int dtype, int topk, cudaStream_t s) {
-  int grid;
-  split_units(p.total_units, p.upc, grid);
+  int sms = num_sms();
+  if (sms <= 0) sms = 1;
+  const int64_t grid0 = std::min<int64_t>(sms, kMaxGrid);
+  int64_t nch = 1;
+  if (p.NR < 2 * grid0) {
+    nch = (4 * grid0 + p.NR - 1) / p.NR;
+    nch = std::max<int64_t>(1, std::min<int64_t>({nch, (int64_t)kMaxChunks, (int64_t)p.upr}));
+  }
+  p.clen = (int)((p.upr + nch - 1) / nch);
+  p.nch = (p.upr + p.clen - 1) / p.clen;  // every chunk non-empty
+  p.nchunks = p.NR * p.nch;
+  const int grid = (int)std::min<int64_t>(grid0, p.nchunks);
   return cuda_status(launch_stream(p, dtype, topk, grid, s));
 }
 

@@ -321,42 +321,39 @@ __device__ __forceinline__ void topk_insert_ordered(float (&tv)[TOPK > 0 ? TOPK 
   }
 }
 
-// Merge the per-lane descending lists of a warp into one list of TOPK,
-// returned identically in every lane (iterative extraction of the warp
-// maximum under a strict total order: value desc, index asc, lane asc).
+// Warp-wide merge of per-lane sorted top lists (value desc, index asc; -inf
+// padding): every lane ends with the first `rounds` (<= TOPK) entries of the
+// merged order, the rest padding.  One round takes the warp maximum of the
+// lanes' heads with two integer reductions (ordered value, then index; an
+// element lives in one list only, so ties between lanes are padding, broken
+// by the lowest lane) and pops it from the winning lane.
 template <int TOPK>
 __device__ __forceinline__ void warp_topk_merge(float (&tv)[TOPK > 0 ? TOPK : 1],
-                                                int (&ti)[TOPK > 0 ? TOPK : 1]) {
+                                                int (&ti)[TOPK > 0 ? TOPK : 1], int rounds) {
   const int lane = threadIdx.x & 31;
   float ov[TOPK > 0 ? TOPK : 1];
   int oi[TOPK > 0 ? TOPK : 1];
 #pragma unroll
   for (int r = 0; r < TOPK; ++r) {
-    float bv = tv[0];
-    int bi = ti[0];
-    int bl = lane;
+    ov[r] = __int_as_float(0xff800000);
+    oi[r] = 0x7fffffff;
+    if (r < rounds) {  // warp-uniform
+      const uint32_t key = ord_float(tv[0]);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const bool head = key == kmax;
+      const uint32_t imin = __reduce_min_sync(0xffffffffu, head ? (uint32_t)ti[0] : 0xffffffffu);
+      const unsigned win = __ballot_sync(0xffffffffu, head && (uint32_t)ti[0] == imin);
+      ov[r] = unord_float(kmax);
+      oi[r] = (int)imin;
+      if (lane == __ffs(win) - 1) {  // pop the head of the winning lane's list
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
-      const int l2 = __shfl_xor_sync(0xffffffffu, bl, off);
-      const bool take = v2 > bv || (v2 == bv && (i2 < bi || (i2 == bi && l2 < bl)));
-      if (take) {
-        bv = v2;
-        bi = i2;
-        bl = l2;
+        for (int k = 0; k < TOPK - 1; ++k) {
+          tv[k] = tv[k + 1];
+          ti[k] = ti[k + 1];
+        }
+        tv[TOPK - 1] = __int_as_float(0xff800000);
+        ti[TOPK - 1] = 0x7fffffff;
       }
-    }
-    ov[r] = bv;
-    oi[r] = bi;
-    if (lane == bl) {  // pop the head of the winning lane's list
-#pragma unroll
-      for (int k = 0; k < TOPK - 1; ++k) {
-        tv[k] = tv[k + 1];
-        ti[k] = ti[k + 1];
-      }
-      tv[TOPK - 1] = __int_as_float(0xff800000);
-      ti[TOPK - 1] = 0x7fffffff;
     }
   }
 #pragma unroll

@@ -26,6 +26,7 @@ constexpr int kUnitsPerStageB = kConsumerWarps;     // one unit per consumer war
 constexpr int kRingBytesB = 196608;                // bulk-copy ring of the CDF pass
 constexpr int kMaxTopK = 16;                        // per-row candidate list (F + 1 <= 16)
 constexpr int kMaxGrid = 4096;                      // bound on CTAs of one launch
+constexpr int kMaxChunks = 16;                      // bound on chunks per row (streaming pass)
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
 
 enum Mode : int { kModeVerify = 0, kModeTopF = 1, kModeSaguaro = 2 };
@@ -77,7 +78,12 @@ struct StreamParams {
   int64_t NR;               // rows in total
   int upr;                  // units per row
   int64_t total_units;
-  int64_t upc;              // units per CTA
+  // Rows are cut into nch chunks of clen units (the last one shorter); CTAs
+  // take chunks in the order (chunk of row, row) from a global counter.
+  int nch, clen;
+  int64_t nchunks;
+  unsigned long long* chunk_ctr;
+  uint32_t* row_cut;        // per row: ordered-float lower bound on its top-list cut (0: none)
   float c;                  // log2(e) / T
   float C;
   int F[SSD_MAX_K + 1];
@@ -94,7 +100,7 @@ struct StreamParams {
   int Fmax;
   int* row_cnt;
   int* grp_cnt;
-  RowPartial* partials;     // slot (row + cta)
+  RowPartial* partials;     // slot row * nch + chunk of row
   RowResult* rowres;
   GroupParams* gparams;
   int32_t* status;
@@ -137,6 +143,7 @@ struct CdfParams {
 // ---- workspace layout ----------------------------------------------------------
 struct WsLayout {
   size_t cnt_off, cnt_bytes;       // counters (cleared each call)
+  size_t ctr_off;                  // chunk counter, within the counters
   size_t part_off, rowres_off, gp_off, sub_off, dbg_off, total;
   int64_t NR;
   int groups, nsub;
@@ -149,11 +156,14 @@ inline WsLayout ws_layout(int groups, int rpg, int V) {
   L.groups = groups;
   L.NR = (int64_t)groups * rpg;
   L.nsub = (V + kUnitB - 1) / kUnitB;
-  size_t ncnt = (size_t)L.NR + 2 * (size_t)groups;
+  // counters: row arrivals [NR], group arrivals [groups], CDF arrivals
+  // [groups], row cuts [NR], then the 8-byte chunk counter
+  size_t ncnt = 2 * (size_t)L.NR + 2 * (size_t)groups;
   L.cnt_off = 0;
-  L.cnt_bytes = align256(ncnt * sizeof(int));
+  L.ctr_off = (ncnt * sizeof(int) + 7) & ~(size_t)7;
+  L.cnt_bytes = align256(L.ctr_off + sizeof(unsigned long long));
   L.part_off = L.cnt_bytes;
-  L.rowres_off = L.part_off + align256(((size_t)L.NR + kMaxGrid) * sizeof(RowPartial));
+  L.rowres_off = L.part_off + align256((size_t)L.NR * kMaxChunks * sizeof(RowPartial));
   L.gp_off = L.rowres_off + align256((size_t)L.NR * sizeof(RowResult));
   L.sub_off = L.gp_off + align256((size_t)groups * sizeof(GroupParams));
   L.dbg_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));

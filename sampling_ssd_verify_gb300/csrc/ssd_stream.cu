@@ -37,6 +37,7 @@ constexpr float kPosInf = INFINITY;
 
 template <int TOPK>
 struct alignas(16) PieceRed {
+  long long chunk;  // the piece's chunk, -1: no more pieces
   float m[kConsumerWarps];
   float hi[kConsumerWarps];
   float lo[kConsumerWarps];
@@ -483,27 +484,42 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
 }
 
 // Warp roles: warps 0..kConsumerWarps-1 reduce staged data, warp
-// kConsumerWarps issues the bulk copies, warp kConsumerWarps+1 merges each row
-// piece's per-warp results and does all global-memory epilogue work, so the
-// consumer warps never wait for it.  Piece results pass through a queue of
-// kPieceSlots shared-memory slots guarded by mbarriers.
+// kConsumerWarps takes chunks from the global counter and issues their bulk
+// copies, and kEpilogueWarps epilogue warps (piece p to warp p mod
+// kEpilogueWarps) merge each piece's per-warp results and do all
+// global-memory epilogue work, so the consumer warps never wait for it.
+// Piece results pass through a queue of kPieceSlots shared-memory slots
+// guarded by mbarriers.
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kEpilogueWarp = kConsumerWarps + 1;
-constexpr int kStreamThreads = (kConsumerWarps + 2) * 32;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;  // the first epilogue warp
+constexpr int kEpilogueWarps = 2;
+constexpr int kStreamThreads = (kConsumerWarps + 1 + kEpilogueWarps) * 32;
 constexpr int kPieceSlots = 4;
+static_assert(kPieceSlots % kEpilogueWarps == 0, "a slot belongs to one epilogue warp");
+// Chunk of each piece, written by the producer before the piece's first
+// stage is published.  The producer runs at most kStagesA + 1 pieces ahead
+// of the consumer warps, so a queue this long is never overwritten early.
+constexpr int kPieceQueue = 16;
+static_assert(kPieceQueue > kStagesA + 1, "piece queue shorter than the pipeline");
 
-// The row pieces of one CTA, in order: [u, ure) units of row `row`.
-struct PieceIter {
-  int64_t u, u_end, upr;
-  __device__ __forceinline__ bool next(int64_t& row, int64_t& pu0, int64_t& pu1) {
-    if (u >= u_end) return false;
-    row = u / upr;
-    pu0 = u;
-    pu1 = min((row + 1) * upr, u_end);
-    u = pu1;
-    return true;
-  }
+// A piece as the producer hands it to the consumer warps (chunk -1: the end).
+struct PieceDesc {
+  long long chunk;
+  int64_t row, pu0, pu1;
+  const char* rp;  // element 0 of the row
+  int jr;          // row within its group
+  int kch;         // chunk of the row
 };
+
+// Units [pu0, pu1) of row `row` that chunk c covers (chunks in the order
+// (chunk of row, row), so a row's later chunks start long after its first).
+__device__ __forceinline__ void chunk_geom(const StreamParams& p, long long c, int64_t& row,
+                                           int& k, int64_t& pu0, int64_t& pu1) {
+  k = (int)(c / p.NR);
+  row = c - (int64_t)k * p.NR;
+  pu0 = row * p.upr + (int64_t)k * p.clen;
+  pu1 = min(pu0 + p.clen, (row + 1) * p.upr);
+}
 
 template <int DT, int TOPK>
 __global__ void __launch_bounds__(kStreamThreads, 1)
@@ -516,17 +532,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   uint64_t* pempty = pfull + kPieceSlots;
   PieceRed<TOPK>* slots = reinterpret_cast<PieceRed<TOPK>*>(pempty + kPieceSlots);
   __shared__ int s_err;
-  // Top-list pruning bound shared by the CTA's warps: (row << 32) | ordered
-  // float.  Rows only increase within a CTA, so a value of another row is
-  // never mistaken for the current row's.
+  // Top-list pruning bound shared by the CTA's warps: (piece << 32) |
+  // ordered float.  Piece numbers only increase within a CTA, so a value of
+  // another piece is never mistaken for the current piece's.
   __shared__ unsigned long long s_cut;
+  __shared__ PieceDesc s_pq[kPieceQueue];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int64_t u_begin = (int64_t)blockIdx.x * p.upc;
-  const int64_t u_end = min(u_begin + p.upc, p.total_units);
-  if (u_begin >= u_end) return;
   constexpr int ups = kStageBytes / (kUnitA * Elem<DT>::kSize);  // units per stage
 
   if (tid == 0) {
@@ -548,10 +562,31 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     // ---------------- producer ----------------
     if (lane == 0) {
       int n = 0;
-      PieceIter it{u_begin, u_end, p.upr};
-      int64_t row, pu0, pu1;
-      while (it.next(row, pu0, pu1)) {
+      unsigned long long next = atomicAdd(p.chunk_ctr, 1ull);
+      for (int piece = 0;; ++piece) {
+        const long long c = next < (unsigned long long)p.nchunks ? (long long)next : -1ll;
+        PieceDesc& d = s_pq[piece % kPieceQueue];
+        d.chunk = c;
+        if (c < 0) {
+          // end marker: one stage without data
+          const int slot = n % kStagesA;
+          if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+          mbar_arrive(full + slot);
+          ++n;
+          break;
+        }
+        next = atomicAdd(p.chunk_ctr, 1ull);  // the following chunk, fetched early
+        int64_t row, pu0, pu1;
+        int k;
+        chunk_geom(p, c, row, k, pu0, pu1);
         const RowGeom rg = row_geom<DT>(p, row);
+        // published to the consumers by the arrival on the piece's first stage
+        d.row = row;
+        d.pu0 = pu0;
+        d.pu1 = pu1;
+        d.rp = rg.rp;
+        d.jr = (int)(row - (row / p.rpg) * p.rpg);
+        d.kch = k;
         for (int64_t u = pu0, un = 0; u < pu1; u = un) {
           un = min(u + ups, pu1);
           const Stage st = stage_of<DT>(rg, p.V, u, un);
@@ -579,18 +614,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   }
 
   const float c = p.c;
-  if (warp == kEpilogueWarp) {
+  if (warp >= kEpilogueWarp) {
     // ---------------- epilogue: merge, publish, finalise ----------------
-    PieceIter it{u_begin, u_end, p.upr};
-    int64_t row, pu0, pu1;
-    for (int piece = 0; it.next(row, pu0, pu1); ++piece) {
+    for (int piece = warp - kEpilogueWarp;; piece += kEpilogueWarps) {
       const int slot = piece % kPieceSlots;
-      mbar_wait(pfull + slot, (piece / kPieceSlots) & 1, &s_err, p.status);
+      if (!mbar_wait(pfull + slot, (piece / kPieceSlots) & 1, &s_err, p.status)) break;
       const PieceRed<TOPK>& R = slots[slot];
+      const long long chunk = R.chunk;
+      if (chunk < 0) break;
+      int64_t row, pu0, pu1;
+      int kch;
+      chunk_geom(p, chunk, row, kch, pu0, pu1);
       const int64_t g = row / p.rpg;
       const int jr = (int)(row - g * p.rpg);
       const bool is_t = jr < p.nt;
       const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
+      const int need = top ? p.F[jr - p.nt] + 1 : 0;  // list entries the row needs
       Acc<TOPK> b;
       b.reset();
       if (lane < kConsumerWarps) {
@@ -611,19 +650,26 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       float M, MC, Shi, Slo;
       warp_softmax_merge(b.m, b.mc, b.hi, b.lo, c, M, MC, Shi, Slo);
       if constexpr (TOPK > 0) {
-        if (top) warp_topk_merge<TOPK>(b.tv, b.ti);
+        if (top) warp_topk_merge<TOPK>(b.tv, b.ti, need);
       }
-      const int64_t r0u = row * p.upr;
-      const int64_t c_lo = r0u / p.upc;
-      const int64_t c_hi = (r0u + p.upr - 1) / p.upc;
-      if (c_lo == c_hi) {
+      if (p.nch == 1) {
         finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, b, top);
         continue;
       }
-      // row shared with other CTAs: publish the partial, last arrival merges
-      if (!SSD_CHK(row + blockIdx.x < p.NR + kMaxGrid && row < p.NR, p.dbg, 6, row, blockIdx.x))
-        continue;
-      RowPartial* slotp = p.partials + (row + blockIdx.x);
+      if constexpr (TOPK > 0) {
+        // the chunk's R-th best logit bounds the row's cut: later chunks of
+        // the row start from it
+        if (top && lane == 0) {
+          const int F = p.F[jr - p.nt];
+          float v = kNegInf;
+#pragma unroll
+          for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) v = k == F ? b.tv[k] : v;
+          if (v != kNegInf) atomicMax(p.row_cut + row, ord_float(v));
+        }
+      }
+      // row split into chunks: publish the partial, the last arrival merges
+      if (!SSD_CHK(row < p.NR && kch < p.nch, p.dbg, 6, row, kch)) continue;
+      RowPartial* slotp = p.partials + (row * p.nch + kch);
       if (lane == 0) {
         slotp->m = M;
         slotp->s_hi = Shi;
@@ -637,18 +683,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       int last = 0;
       if (lane == 0) {
         __threadfence();
-        last = atomicAdd(p.row_cnt + row, 1) == (int)(c_hi - c_lo);
+        last = atomicAdd(p.row_cnt + row, 1) == p.nch - 1;
         if (last) __threadfence();
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (!last) continue;
       Acc<TOPK> mrg;
       mrg.reset();
-      for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32)
-        fold_partial<TOPK>(mrg, p.partials + (row + cc), c, top);
+      for (int cc = lane; cc < p.nch; cc += 32)
+        fold_partial<TOPK>(mrg, p.partials + (row * p.nch + cc), c, top);
       warp_softmax_merge(mrg.m, mrg.mc, mrg.hi, mrg.lo, c, M, MC, Shi, Slo);
       if constexpr (TOPK > 0) {
-        if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti);
+        if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti, need);
       }
       finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, mrg, top);
     }
@@ -660,23 +706,45 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   WarpList<(TOPK > 0 ? TOPK : 1)> wl;
   constexpr int VEC = Elem<DT>::kVec;
   int n = 0;
-  PieceIter it{u_begin, u_end, p.upr};
-  int64_t row, pu0, pu1;
-  for (int piece = 0; it.next(row, pu0, pu1); ++piece) {
-    const int64_t g = row / p.rpg;
-    const int jr = (int)(row - g * p.rpg);
+  for (int piece = 0;; ++piece) {
+    // the piece's first stage (or the end marker) publishes its chunk
+    bool ok = mbar_wait(full + (n % kStagesA), (n / kStagesA) & 1, &s_err, p.status);
+    const volatile PieceDesc& d = s_pq[piece % kPieceQueue];
+    const long long chunk = ok ? d.chunk : -1ll;
+    const int ps = piece % kPieceSlots;
+    if (chunk < 0) {
+      // hand an end marker to every epilogue warp (the next kEpilogueWarps pieces)
+      for (int q = piece; q < piece + kEpilogueWarps; ++q) {
+        const int qs = q % kPieceSlots;
+        if (lane == 0 && q >= kPieceSlots)
+          mbar_wait(pempty + qs, ((q / kPieceSlots) - 1) & 1, &s_err, p.status);
+        if (warp == 0 && lane == 0) slots[qs].chunk = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull + qs);
+      }
+      break;
+    }
+    const int64_t row = d.row, pu0 = d.pu0, pu1 = d.pu1;
+    const int kch = d.kch;
+    const int jr = d.jr;
     const bool is_t = jr < p.nt;
     const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
-    const RowGeom rg = row_geom<DT>(p, row);
+    const RowGeom rg{d.rp, row * p.upr, is_t};
     a.reset();
     wl.reset(top ? p.F[jr - p.nt] + 1 : 1);
-    float ccut = kNegInf;       // CTA-wide pruning bound for this row's top list
+    // pruning bound for this row's top list: what earlier chunks of the row
+    // established, then the CTA's warps' cuts
+    float ccut = kNegInf;
+    if (TOPK > 0 && top && kch > 0) {
+      const uint32_t rc = __ldcg(p.row_cut + row);
+      if (rc != 0u) ccut = unord_float(rc);
+    }
     float published = kNegInf;  // this warp's last published cut
     for (int64_t u = pu0, un = 0; u < pu1; u = un) {
       un = min(u + ups, pu1);
       const Stage st = stage_of<DT>(rg, p.V, u, un);
       const int slot = n % kStagesA;
-      mbar_wait(full + slot, (n / kStagesA) & 1, &s_err, p.status);
+      if (u != pu0) mbar_wait(full + slot, (n / kStagesA) & 1, &s_err, p.status);
       const int nvec = (int)((st.a1 - st.a0) >> 4);
       const int ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
       const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
@@ -749,27 +817,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if (lane == 0) mbar_arrive(empty + slot);
       ++n;
       if (TOPK > 0 && top) {
-        // The warp holds TOPK candidates >= its cut cv, so no logit strictly
+        // The warp holds R candidates >= its cut cv, so no logit strictly
         // below the largest cut of the CTA's warps (for this row) can enter
-        // the row's top list.  A warp publishes its cut only when it rose.
-        const unsigned long long tag = (unsigned long long)(uint32_t)row << 32;
-        unsigned long long w = 0ull;
-        if (lane == 0) {
-          if (wl.cv != kNegInf && wl.cv > published) {
-            atomicMax(&s_cut, tag | ord_float(wl.cv));
-            published = wl.cv;
-          }
-          w = *reinterpret_cast<volatile unsigned long long*>(&s_cut);
+        // the row's top list.  A warp publishes its cut only when it rose
+        // (cv is warp-uniform); every lane then reads the CTA-wide value.
+        if (wl.cv != kNegInf && wl.cv > published) {
+          if (lane == 0)
+            atomicMax(&s_cut, ((unsigned long long)(uint32_t)piece << 32) | ord_float(wl.cv));
+          published = wl.cv;
         }
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if ((w >> 32) == (uint32_t)row) ccut = fmaxf(ccut, unord_float((uint32_t)w));
+        __syncwarp();
+        const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(&s_cut);
+        if ((w >> 32) == (uint32_t)piece) ccut = fmaxf(ccut, unord_float((uint32_t)w));
       }
     }
 
     // ---- hand the piece's per-warp results to the epilogue warp ----
     float M, MC, Shi, Slo;
     warp_softmax_merge(a.m, a.mc, a.hi, a.lo, c, M, MC, Shi, Slo);
-    const int ps = piece % kPieceSlots;
     if (lane == 0 && piece >= kPieceSlots)
       mbar_wait(pempty + ps, ((piece / kPieceSlots) - 1) & 1, &s_err, p.status);
     __syncwarp();
@@ -778,6 +843,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       R.m[warp] = M;
       R.hi[warp] = Shi;
       R.lo[warp] = Slo;
+      if (warp == 0) R.chunk = chunk;
     }
     if (lane < (TOPK > 0 ? TOPK : 1)) {
       R.tv[warp][lane] = (TOPK > 0 && top) ? wl.lv : kNegInf;
