@@ -54,16 +54,6 @@ ssd_status cuda_status(cudaError_t e) {
   return SSD_ERR_CUDA;
 }
 
-// Grid for `total` equal units: at most one CTA per SM, equal contiguous shares.
-void split_units(int64_t total, int64_t& upc, int& grid) {
-  int sms = num_sms();
-  if (sms <= 0) sms = 1;
-  int64_t g = std::min<int64_t>({(int64_t)sms, (int64_t)kMaxGrid, total});
-  if (g < 1) g = 1;
-  upc = (total + g - 1) / g;
-  grid = (int)((total + upc - 1) / upc);
-}
-
 struct Common {
   StreamParams sp;
   CdfParams cp;
@@ -135,6 +125,7 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   q.nt = nt;
   q.subsum = reinterpret_cast<float*>(ws + L.sub_off);
   q.cnt = cnt + L.NR + groups;
+  q.chunk_ctr = p.chunk_ctr + 1;
   q.t_lo = p.t_lo;
   q.t_hi = p.t_hi;
   q.d_lo = p.d_lo;
@@ -164,9 +155,18 @@ ssd_status run_stream(StreamParams& p, int dtype, int topk, cudaStream_t s) {
   return cuda_status(launch_stream(p, dtype, topk, grid, s));
 }
 
+// Chunks of the CDF pass: about four per CTA in all, at most four pipeline
+// stages of kUnitsPerStageB units each.
 ssd_status run_cdf(CdfParams& q, int dtype, cudaStream_t s) {
-  int grid;
-  split_units(q.total_units, q.upc, grid);
+  int sms = num_sms();
+  if (sms <= 0) sms = 1;
+  const int64_t grid0 = std::min<int64_t>(sms, kMaxGrid);
+  int64_t cu = (q.total_units + 4 * grid0 - 1) / (4 * grid0);
+  cu = std::max<int64_t>(1, std::min<int64_t>({cu, 4 * (int64_t)kUnitsPerStageB, (int64_t)q.nsub}));
+  q.cu = (int)cu;
+  q.cpg = (q.nsub + q.cu - 1) / q.cu;
+  q.nchunks = (int64_t)q.groups * q.cpg;
+  const int grid = (int)std::min<int64_t>(grid0, q.nchunks);
   return cuda_status(launch_cdf(q, dtype, grid, s));
 }
 

@@ -9,12 +9,13 @@
 // ([SSD-note] §"Saguaro 优化二：Saguaro 采样").  The token drawn is the
 // smallest y with sum_{y'<=y} w(y') > u * Z, Z = sum_y w(y).
 //
-// Work is split into 512-element units over (group, unit); one persistent
-// CTA per SM streams its share of units of the one or two rows a group needs
-// through a bulk-copy ring, each consumer warp reduces one unit to its
-// weight sum, and the last CTA to finish a group (atomic arrival counter)
-// locates the unit holding u*Z by a prefix over the unit sums and scans that
-// unit in vocabulary order.
+// Work is split into 512-element units over (group, unit), and the units of
+// a group into chunks that persistent CTAs (one per SM) take from a global
+// counter.  A CTA streams a chunk of the one or two rows the group needs
+// through a bulk-copy ring, each consumer warp reduces one unit to its weight
+// sum, and the CTA that completes a group (atomic arrival counter) locates
+// the unit holding u*Z by a prefix over the unit sums and scans that unit in
+// vocabulary order.
 //
 // Sources: [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈";
 // [SD-7.3] "7.3 Speculative Decoding：投机采样加速".
@@ -422,50 +423,97 @@ __device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupPa
   }
 }
 
+// Warp roles: warps 0..kConsumerWarps-1 sum units (one unit per warp and
+// stage), warp kConsumerWarps takes chunks from the global counter and issues
+// their bulk copies, and kDrawWarps draw warps (chunk p of the CTA to warp
+// p mod kDrawWarps) count finished chunks into their group's arrival counter
+// and run the draw of the groups they complete, so the consumer warps never
+// wait for a draw.  Chunks go in the order (chunk of group, group): a group
+// is completed by its last chunk, and the draws spread over the CTAs.
+constexpr int kCdfProducer = kConsumerWarps;
+constexpr int kCdfDrawWarp = kConsumerWarps + 1;  // the first draw warp
+constexpr int kDrawWarps = 2;
+constexpr int kCdfThreads = (kConsumerWarps + 1 + kDrawWarps) * 32;
+constexpr int kDrawSlots = 8;   // chunks the draw warps may lag behind
+static_assert(kDrawSlots % kDrawWarps == 0, "a slot belongs to one draw warp");
+constexpr int kCdfQueue = 32;   // chunk descriptors in flight
+
+// A chunk as the producer hands it on (chunk -1: the end).
+struct CdfDesc {
+  long long chunk;
+  int64_t g;       // group
+  int u0, u1;      // units [u0, u1) of the group
+  GroupParams gp;  // the group's draw parameters
+};
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) cdf_kernel(const __grid_constant__ CdfParams p) {
+__global__ void __launch_bounds__(kCdfThreads, 1) cdf_kernel(const __grid_constant__ CdfParams p) {
   constexpr int ES = Elem<DT>::kSize;
   constexpr int HALF = CdfRing<DT>::HALF;
   constexpr int STAGE = CdfRing<DT>::STAGE;
   constexpr int kStagesB = CdfRing<DT>::NST;
+  static_assert(kCdfQueue > kStagesB + 1 + kDrawSlots, "descriptor queue too short");
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesB * STAGE);
   uint64_t* empty = full + kStagesB;
+  uint64_t* cdone = empty + kStagesB;
+  uint64_t* cempty = cdone + kDrawSlots;
   __shared__ int s_err;
+  __shared__ CdfDesc s_q[kCdfQueue];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int64_t u_begin = (int64_t)blockIdx.x * p.upc;
-  const int64_t u_end = min(u_begin + p.upc, p.total_units);
-  if (u_begin >= u_end) return;
 
   if (tid == 0) {
     for (int i = 0; i < kStagesB; ++i) {
       mbar_init(full + i, 1);
       mbar_init(empty + i, kConsumerWarps);
     }
+    for (int i = 0; i < kDrawSlots; ++i) {
+      mbar_init(cdone + i, kConsumerWarps);
+      mbar_init(cempty + i, 1);
+    }
     s_err = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == kCdfProducer) {
+    // ---------------- producer ----------------
     if (lane == 0) {
       int n = 0;
-      for (int64_t u = u_begin; u < u_end;) {
-        const int64_t g = u / p.nsub;
-        const int64_t uge = min((g + 1) * (int64_t)p.nsub, u_end);
-        if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) break;
-        const GroupParams& gp = p.gp[g];
-        const int use_t = gp.use_t, use_d = gp.use_d;
-        const char* rt = use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;
-        const char* rd = use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, ES) : nullptr;
-        for (int64_t un = 0; u < uge; u = un) {
-          un = min(u + (int64_t)kUnitsPerStageB, uge);
-          const int e0 = (int)((u - g * p.nsub) * kUnitB);
-          const int e1 = (int)min((int64_t)p.V, (un - g * p.nsub) * kUnitB);
+      unsigned long long next = atomicAdd(p.chunk_ctr, 1ull);
+      for (int piece = 0;; ++piece) {
+        const long long c = next < (unsigned long long)p.nchunks ? (long long)next : -1ll;
+        CdfDesc& d = s_q[piece % kCdfQueue];
+        d.chunk = c;
+        if (c >= 0) {
+          const int kc = (int)(c / p.groups);
+          const int64_t g = c - (int64_t)kc * p.groups;
+          if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) d.chunk = -1;
+          d.g = g;
+          d.u0 = kc * p.cu;
+          d.u1 = min(d.u0 + p.cu, p.nsub);
+        }
+        if (d.chunk < 0) {
+          // end marker: one stage without data
+          const int slot = n % kStagesB;
+          if (n >= kStagesB) mbar_wait(empty + slot, ((n / kStagesB) - 1) & 1, &s_err, p.status);
+          mbar_arrive(full + slot);
+          ++n;
+          break;
+        }
+        next = atomicAdd(p.chunk_ctr, 1ull);  // the following chunk, fetched early
+        const GroupParams gp = p.gp[d.g];
+        d.gp = gp;  // published by the arrival on the chunk's first stage
+        const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;
+        const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, ES) : nullptr;
+        for (int u = d.u0, un = 0; u < d.u1; u = un) {
+          un = min(u + kUnitsPerStageB, d.u1);
+          const int e0 = u * kUnitB;
+          const int e1 = min(p.V, un * kUnitB);
           const int slot = n % kStagesB;
           if (n >= kStagesB) mbar_wait(empty + slot, ((n / kStagesB) - 1) & 1, &s_err, p.status);
           uintptr_t a0[2] = {0, 0}, a1[2] = {0, 0};
@@ -496,98 +544,127 @@ __global__ void __launch_bounds__(kThreads, 1) cdf_kernel(const __grid_constant_
           ++n;
         }
       }
+      // do not leave while copies into this CTA's shared memory are in flight
       for (int q = max(0, n - kStagesB); q < n; ++q)
         mbar_wait(full + (q % kStagesB), (q / kStagesB) & 1, &s_err, p.status);
     }
     return;
   }
 
-  // ---------------- consumers ----------------
-  int n = 0;
-  for (int64_t u = u_begin; u < u_end;) {
-    const int64_t g = u / p.nsub;
-    const int64_t uge = min((g + 1) * (int64_t)p.nsub, u_end);
-    const int64_t ug0 = u;
-    const GroupParams gp = p.gp[g];
-    const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;
-    const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, ES) : nullptr;
-    for (int64_t un = 0; u < uge; u = un) {
-      un = min(u + (int64_t)kUnitsPerStageB, uge);
-      const int e0 = (int)((u - g * p.nsub) * kUnitB);
-      const int e1 = (int)min((int64_t)p.V, (un - g * p.nsub) * kUnitB);
-      const int slot = n % kStagesB;
-      mbar_wait(full + slot, (n / kStagesB) & 1, &s_err, p.status);
-      Half ht, hd;
-      for (int h = 0; h < 2; ++h) {
-        Half& H = h == 0 ? ht : hd;
-        const char* r = h == 0 ? rt : rd;
-        H.row = r;
-        H.sm = reinterpret_cast<const char*>(ring + slot * STAGE + h * HALF);
-        H.ei0 = H.ei1 = e0;
-        if (r != nullptr) {
-          const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
-          const uintptr_t b1 = (uintptr_t)(r + (int64_t)e1 * ES);
-          const uintptr_t A0 = (b0 + 15) & ~(uintptr_t)15;
-          const uintptr_t A1 = b1 & ~(uintptr_t)15;
-          if (A1 > A0) {
-            H.ei0 = e0 + (int)((A0 - b0) / ES);
-            H.ei1 = H.ei0 + (int)((A1 - A0) / ES);
-          }
-        }
-      }
-      const int64_t uu = u + warp;
-      if (uu < un) {
-        const int ue0 = (int)((uu - g * p.nsub) * kUnitB);
-        const int ue1 = min(ue0 + kUnitB, p.V);
-        constexpr int VEC = Elem<DT>::kVec;
-        bool fast = ue1 - ue0 == kUnitB;
-        if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
-        if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
-        float s = 0.f;
-        if (fast) {
-          s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
-        } else {
-          for (int m = 0; m < kUnitB / 32; ++m) {
-            const int y = ue0 + lane + 32 * m;
-            if (y < ue1) {
-              const float zt = gp.use_t ? fetch<DT>(ht, y, p, true) : 0.f;
-              const float zd = gp.use_d ? fetch<DT>(hd, y, p, false) : 0.f;
-              s += weight(gp, p.c, y, zt, zd);
-            }
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0 && SSD_CHK(uu < (int64_t)p.groups * p.nsub, p.dbg, 23, uu, g))
-          p.subsum[g * p.nsub + (uu - g * p.nsub)] = s;
-      }
+  if (warp >= kCdfDrawWarp) {
+    // ---------------- draw: group arrival, then the draw ----------------
+    for (int piece = warp - kCdfDrawWarp;; piece += kDrawWarps) {
+      const int ds = piece % kDrawSlots;
+      if (!mbar_wait(cdone + ds, (piece / kDrawSlots) & 1, &s_err, p.status)) break;
+      const CdfDesc& d = s_q[piece % kCdfQueue];
+      const long long chunk = d.chunk;
+      const int64_t g = d.g;
+      const int nu = d.u1 - d.u0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty + slot);
-      ++n;
-    }
-    // this CTA's units of group g are summed: arrival
-    consumer_sync();
-    if (warp == 0) {
+      if (lane == 0) mbar_arrive(cempty + ds);
+      if (chunk < 0) break;
+      // this chunk's unit sums are written: count them into the group
       int last = 0;
       if (lane == 0) {
         __threadfence();
-        last = SSD_CHK(g < p.groups, p.dbg, 28, g, p.groups)
-                   ? atomicAdd(p.cnt + g, (int)(uge - ug0)) + (int)(uge - ug0) == p.nsub
-                   : 0;
+        last = atomicAdd(p.cnt + g, nu) + nu == p.nsub;
         if (last) __threadfence();
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) group_draw<DT>(p, g);
     }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  int n = 0;
+  for (int piece = 0;; ++piece) {
+    // the chunk's first stage (or the end marker) publishes its descriptor
+    const bool ok = mbar_wait(full + (n % kStagesB), (n / kStagesB) & 1, &s_err, p.status);
+    const CdfDesc& d = s_q[piece % kCdfQueue];
+    const long long chunk = ok ? d.chunk : -1ll;
+    if (chunk >= 0) {
+      const int64_t g = d.g;
+      const int u0 = d.u0, u1 = d.u1;
+      const GroupParams gp = d.gp;
+      const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;
+      const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, ES) : nullptr;
+      for (int u = u0, un = 0; u < u1; u = un) {
+        un = min(u + kUnitsPerStageB, u1);
+        const int e0 = u * kUnitB;
+        const int e1 = min(p.V, un * kUnitB);
+        const int slot = n % kStagesB;
+        if (u != u0) mbar_wait(full + slot, (n / kStagesB) & 1, &s_err, p.status);
+        Half ht, hd;
+        for (int h = 0; h < 2; ++h) {
+          Half& H = h == 0 ? ht : hd;
+          const char* r = h == 0 ? rt : rd;
+          H.row = r;
+          H.sm = reinterpret_cast<const char*>(ring + slot * STAGE + h * HALF);
+          H.ei0 = H.ei1 = e0;
+          if (r != nullptr) {
+            const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
+            const uintptr_t b1 = (uintptr_t)(r + (int64_t)e1 * ES);
+            const uintptr_t A0 = (b0 + 15) & ~(uintptr_t)15;
+            const uintptr_t A1 = b1 & ~(uintptr_t)15;
+            if (A1 > A0) {
+              H.ei0 = e0 + (int)((A0 - b0) / ES);
+              H.ei1 = H.ei0 + (int)((A1 - A0) / ES);
+            }
+          }
+        }
+        const int uu = u + warp;
+        if (uu < un) {
+          const int ue0 = uu * kUnitB;
+          const int ue1 = min(ue0 + kUnitB, p.V);
+          constexpr int VEC = Elem<DT>::kVec;
+          bool fast = ue1 - ue0 == kUnitB;
+          if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
+          if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
+          float s = 0.f;
+          if (fast) {
+            s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
+          } else {
+            for (int m = 0; m < kUnitB / 32; ++m) {
+              const int y = ue0 + lane + 32 * m;
+              if (y < ue1) {
+                const float zt = gp.use_t ? fetch<DT>(ht, y, p, true) : 0.f;
+                const float zd = gp.use_d ? fetch<DT>(hd, y, p, false) : 0.f;
+                s += weight(gp, p.c, y, zt, zd);
+              }
+            }
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+          if (lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
+            p.subsum[g * p.nsub + uu] = s;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);
+        ++n;
+      }
+    }
+    // hand the finished chunk (or end markers for every draw warp) on
+    for (int q = piece; q < piece + (chunk < 0 ? kDrawWarps : 1); ++q) {
+      const int qs = q % kDrawSlots;
+      if (lane == 0 && q >= kDrawSlots)
+        mbar_wait(cempty + qs, ((q / kDrawSlots) - 1) & 1, &s_err, p.status);
+      // the producer wrote one end marker; the extra ones are marked here
+      if (q > piece && warp == 0 && lane == 0) s_q[q % kCdfQueue].chunk = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cdone + qs);
+    }
+    if (chunk < 0) break;
   }
 }
 
 }  // namespace
 
 int cdf_smem_bytes(int dtype) {
+  const int bars = 2 * kDrawSlots * (int)sizeof(uint64_t);
   return dtype == SSD_BF16
-             ? CdfRing<0>::NST * CdfRing<0>::STAGE + 2 * CdfRing<0>::NST * (int)sizeof(uint64_t)
-             : CdfRing<1>::NST * CdfRing<1>::STAGE + 2 * CdfRing<1>::NST * (int)sizeof(uint64_t);
+             ? CdfRing<0>::NST * CdfRing<0>::STAGE + 2 * CdfRing<0>::NST * (int)sizeof(uint64_t) + bars
+             : CdfRing<1>::NST * CdfRing<1>::STAGE + 2 * CdfRing<1>::NST * (int)sizeof(uint64_t) + bars;
 }
 
 cudaError_t launch_cdf(const CdfParams& p, int dtype, int grid, cudaStream_t s) {
@@ -596,11 +673,11 @@ cudaError_t launch_cdf(const CdfParams& p, int dtype, int grid, cudaStream_t s) 
   if (dtype == SSD_BF16) {
     e = cudaFuncSetAttribute(cdf_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cdf_kernel<0><<<grid, kThreads, smem, s>>>(p);
+    cdf_kernel<0><<<grid, kCdfThreads, smem, s>>>(p);
   } else {
     e = cudaFuncSetAttribute(cdf_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cdf_kernel<1><<<grid, kThreads, smem, s>>>(p);
+    cdf_kernel<1><<<grid, kCdfThreads, smem, s>>>(p);
   }
   return cudaGetLastError();
 }

@@ -119,7 +119,12 @@ struct CdfParams {
   int64_t d_stride;
   int groups, V, nsub;
   int64_t total_units;
-  int64_t upc;
+  // Each group's nsub units are cut into cpg chunks of cu units (the last one
+  // shorter); CTAs take chunks in the order (chunk of group, group) from a
+  // global counter.
+  int cu, cpg;
+  int64_t nchunks;
+  unsigned long long* chunk_ctr;
   float c;
   int mode;
   const GroupParams* gp;
@@ -143,7 +148,7 @@ struct CdfParams {
 // ---- workspace layout ----------------------------------------------------------
 struct WsLayout {
   size_t cnt_off, cnt_bytes;       // counters (cleared each call)
-  size_t ctr_off;                  // chunk counter, within the counters
+  size_t ctr_off;                  // chunk counters (streaming, CDF pass), within the counters
   size_t part_off, rowres_off, gp_off, sub_off, dbg_off, total;
   int64_t NR;
   int groups, nsub;
@@ -157,11 +162,11 @@ inline WsLayout ws_layout(int groups, int rpg, int V) {
   L.NR = (int64_t)groups * rpg;
   L.nsub = (V + kUnitB - 1) / kUnitB;
   // counters: row arrivals [NR], group arrivals [groups], CDF arrivals
-  // [groups], row cuts [NR], then the 8-byte chunk counter
+  // [groups], row cuts [NR], then the 8-byte chunk counters of both passes
   size_t ncnt = 2 * (size_t)L.NR + 2 * (size_t)groups;
   L.cnt_off = 0;
   L.ctr_off = (ncnt * sizeof(int) + 7) & ~(size_t)7;
-  L.cnt_bytes = align256(L.ctr_off + sizeof(unsigned long long));
+  L.cnt_bytes = align256(L.ctr_off + 2 * sizeof(unsigned long long));  // stream, CDF
   L.part_off = L.cnt_bytes;
   L.rowres_off = L.part_off + align256((size_t)L.NR * kMaxChunks * sizeof(RowPartial));
   L.gp_off = L.rowres_off + align256((size_t)L.NR * sizeof(RowResult));
