@@ -161,6 +161,101 @@ __device__ int full_row_draw(const CdfParams& p, const GroupParams& gp, const ch
   return t;
 }
 
+// ---- double-float arithmetic for the draw ------------------------------------------
+// A non-negative value hi + lo held as a normalised pair of floats (|lo| at
+// most half an ulp of hi): about 48 significant bits at any magnitude, on the
+// fp32 pipes.  The draw's sums, prefixes and comparisons use it; sums of
+// non-negative terms only, so the two-sum based add stays accurate.
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF df_of(float x) { return DF{x, 0.f}; }
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  pair_add(a.hi, a.lo, b.hi, b.lo);
+  return a;
+}
+
+// a * u for 0 <= u < 1 (exact product of the high part, then normalised).
+__device__ __forceinline__ DF df_scale(DF a, float u) {
+  const float p = a.hi * u;
+  const float e = fmaf(a.lo, u, fmaf(a.hi, u, -p));
+  DF r;
+  r.hi = p + e;
+  r.lo = e - (r.hi - p);
+  return r;
+}
+
+// a > b for normalised pairs.
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ DF df_shfl(DF v, int src) {
+  return DF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+__device__ __forceinline__ DF df_shfl_up(DF v, int off) {
+  return DF{__shfl_up_sync(0xffffffffu, v.hi, off), __shfl_up_sync(0xffffffffu, v.lo, off)};
+}
+
+// Inclusive warp prefix sum over the first `width` lanes (a power of two;
+// lanes beyond take part with whatever they hold and are ignored).
+__device__ __forceinline__ DF df_warp_scan(DF v, int width = 32) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    if (off >= width) break;
+    const DF o = df_shfl_up(v, off);
+    if (lane >= off) v = df_add(v, o);
+  }
+  return v;
+}
+
+// Pairwise sum of 16 floats (depth 4).
+__device__ __forceinline__ DF df_sum16(const float* x) {
+  DF t[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float s, e;
+    two_sum(x[2 * k], x[2 * k + 1], s, e);
+    t[k].hi = s + e;
+    t[k].lo = e - (t[k].hi - s);
+  }
+#pragma unroll
+  for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+    for (int k = 0; k < w; ++k) t[k] = df_add(t[k], t[k + w]);
+  return t[0];
+}
+
+// Lane L's 16 values x[0..15], in order: the first k with x[k] > 0 and
+// base + x[0] + ... + x[k] > thr, found with lanes 0..15 holding one value
+// each (a shuffle per value, then a 16-lane scan).  Returns k, or -1 if no
+// prefix exceeds thr; *before gets base + x[0] + ... + x[k-1], and *lastpos
+// the last k with x[k] > 0 (-1 if none).  Called by all 32 lanes.
+__device__ __forceinline__ int lane_search16(const float* x, int L, DF base, DF thr, DF* before,
+                                             int* lastpos) {
+  const int lane = threadIdx.x & 31;
+  float mine = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float o = __shfl_sync(0xffffffffu, x[k], L);
+    if (lane == k) mine = o;
+  }
+  const DF incl = df_warp_scan(df_of(lane < 16 ? mine : 0.f), 16);
+  const DF up = df_shfl_up(incl, 1);  // every lane takes part in the shuffle
+  const DF excl = lane == 0 ? DF{0.f, 0.f} : up;
+  const unsigned pos = __ballot_sync(0xffffffffu, lane < 16 && mine > 0.f);
+  const unsigned hit =
+      __ballot_sync(0xffffffffu, lane < 16 && mine > 0.f && df_gt(df_add(base, incl), thr));
+  *lastpos = pos ? 31 - __clz(pos) : -1;
+  const int k = hit ? __ffs(hit) - 1 : -1;
+  *before = df_add(base, df_shfl(excl, k >= 0 ? k : 0));
+  return k;
+}
+
 // Sixteen consecutive logits of row `r` starting at y0 (< e1), vectorised
 // when the address is 16-byte aligned and the run is complete.
 template <int DT>
@@ -187,21 +282,20 @@ __device__ __forceinline__ void load16(const CdfParams& p, const char* r, bool i
   }
 }
 
-// The draw for group g (warp 0 of the last CTA to finish the group).
-// 1. Z = sum of the group's unit sums (each lane loads 16 units at once).
-// 2. The unit holding u*Z: lane prefix in registers + warp scan (fp64).
+// The draw for group g (one warp of the CTA that completes the group).
+// 1. Z = sum of the group's unit sums (each lane holds 16 units at once).
+// 2. The unit holding u*Z: lane prefix + warp scan, then inside the lane
+//    that crosses u*Z.
 // 3. Inside that unit: each lane takes 16 consecutive tokens, lane prefix +
 //    warp scan in vocabulary order; the first token whose cumulative weight
-//    exceeds the remainder is the draw.
+//    exceeds u*Z is the draw.
+// Sums and prefixes are double-float pairs (see DF); a row whose weights
+// vanish in rounding falls back to the fp64 two-pass draw.
 template <int DT>
 __device__ void group_draw(const CdfParams& p, int64_t g) {
   constexpr int R = 16;  // unit sums per lane per round
   const int lane = threadIdx.x & 31;
   if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) return;
-  const GroupParams gp = p.gp[g];
-  const int esz = Elem<DT>::kSize;
-  const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, esz) : nullptr;
-  const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, esz) : nullptr;
   const float* sub = p.subsum + g * p.nsub;
   const int nsub = p.nsub;
   const int rounds = (nsub + 32 * R - 1) / (32 * R);
@@ -214,18 +308,27 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
                  ? __ldcg(sub + u) : 0.f;
     }
   };
-  double Zl = 0.0;
-  for (int rnd = 0; rnd < rounds; ++rnd) {
+  load_round(0);  // in flight together with the group's parameters
+  const GroupParams gp = p.gp[g];
+  const int esz = Elem<DT>::kSize;
+  const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, esz) : nullptr;
+  const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, esz) : nullptr;
+  DF loc0 = df_sum16(v);  // round 0's lane sum, reused by the search
+  DF Zl = loc0;
+  for (int rnd = 1; rnd < rounds; ++rnd) {
     load_round(rnd);
-#pragma unroll
-    for (int k = 0; k < R; ++k) Zl += (double)v[k];
+    Zl = df_add(Zl, df_sum16(v));
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) Zl += __shfl_xor_sync(0xffffffffu, Zl, off);
-  double Z = Zl;
+  for (int off = 16; off > 0; off >>= 1) {
+    const DF o{__shfl_xor_sync(0xffffffffu, Zl.hi, off), __shfl_xor_sync(0xffffffffu, Zl.lo, off)};
+    Zl = df_add(Zl, o);
+  }
+  const DF Z = Zl;  // the same in every lane (the pairwise adds commute)
+  double Zd = (double)Z.hi + (double)Z.lo;
   int t;
   float wt;
-  if (!(Z > 1e-30)) {
+  if (!(Zd > 1e-30)) {
     // The residual vanished in rounding (exact arithmetic forbids it after a
     // rejection): draw the bonus from p_k instead and report it.
     if (lane == 0 && p.status) atomicOr(p.status, SSD_DEV_ZERO_RESIDUAL);
@@ -235,49 +338,42 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
       gp2.use_d = 1;
       gp2.sign_d = 1;
     }
-    t = full_row_draw<DT>(p, gp2, rt, rd, &Z);
+    t = full_row_draw<DT>(p, gp2, rt, rd, &Zd);
     wt = weight_global<DT>(p, gp2, rt, rd, t);
   } else {
-    const double thr = gp.u * Z;
+    // u has 24 fraction bits: exact as a float
+    const DF thr = df_scale(Z, (float)gp.u);
     int unit = -1;
-    double before = 0.0;
-    double run = 0.0;
+    DF before{0.f, 0.f};
+    bool any_before = true;  // false: take the last positive weight
+    DF run{0.f, 0.f};
     for (int rnd = 0; rnd < rounds && unit < 0; ++rnd) {
-      if (rounds > 1) load_round(rnd);
-      double loc = 0.0;
-#pragma unroll
-      for (int k = 0; k < R; ++k) loc += (double)v[k];
-      const double incl = warp_incl_scan(loc);
-      const unsigned m = __ballot_sync(0xffffffffu, run + incl > thr);
+      DF loc = loc0;
+      if (rounds > 1) {  // v holds the last round's sums after Z
+        load_round(rnd);
+        if (rnd > 0) loc = df_sum16(v);
+      }
+      const DF incl = df_warp_scan(loc);
+      const DF up = df_shfl_up(incl, 1);
+      const DF excl = lane == 0 ? DF{0.f, 0.f} : up;
+      const unsigned m = __ballot_sync(0xffffffffu, df_gt(df_add(run, incl), thr));
       if (m) {
         const int L = __ffs(m) - 1;
-        int uk = -1;
-        double bk = 0.0;
-        if (lane == L) {
-          double acc = run + (incl - loc);
-#pragma unroll
-          for (int k = 0; k < R; ++k) {
-            if (uk < 0 && v[k] > 0.f && acc + (double)v[k] > thr) {
-              uk = k;
-              bk = acc;
-            }
-            acc += (double)v[k];
-          }
-          if (uk < 0) {  // rounding inside the lane: its last positive unit
-#pragma unroll
-            for (int k = 0; k < R; ++k)
-              if (v[k] > 0.f) uk = k;
-            bk = -INFINITY;
-          }
+        // prefix before lane L's first unit
+        const DF base = df_add(run, df_shfl(excl, L));
+        DF bk;
+        int lastk;
+        int uk = lane_search16(v, L, base, thr, &bk, &lastk);
+        if (uk < 0) {  // rounding inside the lane: its last positive unit
+          uk = lastk;
+          any_before = false;
         }
-        uk = __shfl_sync(0xffffffffu, uk, L);
-        bk = __shfl_sync(0xffffffffu, bk, L);
         if (uk >= 0) {
           unit = rnd * 32 * R + L * R + uk;
           before = bk;
         }
       }
-      run += __shfl_sync(0xffffffffu, incl, 31);
+      run = df_add(run, df_shfl(incl, 31));
     }
     if (unit < 0) {  // no prefix exceeded u*Z: the last unit with weight
       int cand = -1;
@@ -291,7 +387,7 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
       for (int off = 16; off > 0; off >>= 1)
         cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
       unit = cand >= 0 ? cand : nsub - 1;
-      before = -INFINITY;  // no index qualifies: the last positive weight is taken
+      any_before = false;
     }
     // vocabulary-order scan of the unit: lane l holds tokens e0 + 16 l ...
     const int e0 = unit * kUnitB;
@@ -302,35 +398,25 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
     for (int k = 0; k < 16; ++k) zt[k] = zd[k] = 0.f;
     if (gp.use_t) load16<DT>(p, rt, true, y0, e1, zt);
     if (gp.use_d) load16<DT>(p, rd, false, y0, e1, zd);
-    double loc = 0.0;
     int lastpos = -1;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       w[k] = y0 + k < e1 ? weight(gp, p.c, y0 + k, zt[k], zd[k]) : 0.f;
-      loc += (double)w[k];
       if (w[k] > 0.f) lastpos = y0 + k;
     }
-    const double incl = warp_incl_scan(loc);
-    const double rem = thr - before;
-    const unsigned m = __ballot_sync(0xffffffffu, incl > rem);
+    const DF incl = df_warp_scan(df_sum16(w));
+    const DF up = df_shfl_up(incl, 1);
+    const DF excl = lane == 0 ? DF{0.f, 0.f} : up;
     t = -1;
-    wt = 0.f;
+    const unsigned m =
+        __ballot_sync(0xffffffffu, any_before && df_gt(df_add(before, incl), thr));
     if (m) {
       const int L = __ffs(m) - 1;
-      int tk = -1;
-      if (lane == L) {
-        double acc = incl - loc;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          if (tk < 0 && w[k] > 0.f && acc + (double)w[k] > rem) tk = k;
-          acc += (double)w[k];
-        }
-        if (tk < 0)
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            if (w[k] > 0.f) tk = k;
-      }
-      tk = __shfl_sync(0xffffffffu, tk, L);
+      const DF base = df_add(before, df_shfl(excl, L));
+      DF bt;
+      int lastk;
+      int tk = lane_search16(w, L, base, thr, &bt, &lastk);
+      if (tk < 0) tk = lastk;  // rounding inside the lane: its last positive weight
       if (tk >= 0) t = e0 + L * 16 + tk;
     }
     if (t < 0) {  // rounding left no index: the last positive weight of the unit
@@ -349,8 +435,8 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   if (lane != 0) return;
   if (!SSD_CHK(g < p.groups && t >= 0 && t < p.V, p.dbg, 25, g, t)) return;
   p.out_token[g] = t;
-  if (p.out_mass) p.out_mass[g] = (float)Z;
-  if (p.out_qprime) p.out_qprime[g] = (float)((double)wt / Z);
+  if (p.out_mass) p.out_mass[g] = (float)Zd;
+  if (p.out_qprime) p.out_qprime[g] = (float)((double)wt / Zd);
   if (p.out_guess) {
     const RowResult* rr = p.rowres + g * p.rpg + p.nt;
     int n = 0;

@@ -151,6 +151,10 @@ EDGES = [
     Edge("F up to 15", 6, 2, 700, "bf16", (15, 9, 4), C=0.2),
     Edge("high temperature", 30, 4, 2048, "f32", (3, 3, 2, 2, 2), T=2.5),
     Edge("low temperature", 30, 4, 2048, "bf16", (3, 3, 2, 2, 2), T=0.3),
+    # more than 512 draw units per row: the bonus draw sums and searches its
+    # unit sums in several rounds
+    Edge("V300000 multi-round draw f32", 6, 3, 300000, "f32", (3, 2, 2, 1)),
+    Edge("V300000 multi-round draw bf16", 6, 3, 300000, "bf16", (3, 2, 2, 1), C=1.0),
 ]
 
 
