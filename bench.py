@@ -140,6 +140,29 @@ def dist_env():
     return world, rank, local
 
 
+# Multi-GPU runs are replicas: every rank verifies its own batch (independent
+# sequences, so the path has no data exchange), the step time is the slowest
+# rank's, and the throughput counts every rank's rows (weak scaling).
+def rank_seed(w, rank):
+    """Seed of rank `rank`'s synthetic batch (distinct per rank)."""
+    return w.seed + 7919 * rank
+
+
+def max_over_ranks(x, tdist, device=None):
+    """The maximum of a per-rank float over all ranks (x itself on one rank)."""
+    import torch
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank, world, seconds):
+    """Whole-job throughput: rows verified by all ranks per second."""
+    return rows_per_rank * world / seconds
+
+
 # ------------------------------------------------------------------------------ ours
 def run_ours(args):
     import torch
@@ -160,7 +183,7 @@ def run_ours(args):
                                 name=f"{w.name} [B={args.batch or w.B}, V={args.vocab or w.V}]")
     B, K, Kq, V = w.B, w.K, w.Kq, w.V
     F = np.asarray(w.fanout, dtype=np.int32)
-    bt = make_batch(w, seed=w.seed + 7919 * rank)
+    bt = make_batch(w, seed=rank_seed(w, rank))
     if w.dtype == "bf16":
         tg = torch.from_numpy(bt["target"].view(np.int16)).to(dev).view(torch.bfloat16)
         dg = torch.from_numpy(bt["draft"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -216,11 +239,7 @@ def run_ours(args):
     if world > 1:
         tdist.barrier()
     ck = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), tdist, dev)
     ms_step = ms / args.steps
     verify_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_v]))
     alg = w.algorithmic_bytes()
@@ -270,15 +289,12 @@ def run_ours(args):
         w0 = time.perf_counter()
         for s in range(ne):
             e2e_step(90_000 + s)
-        e2e_s = time.perf_counter() - w0
-        if world > 1:
-            tt = torch.tensor([e2e_s], device=dev)
-            tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-            e2e_s = float(tt.item())
+        e2e_s = max_over_ranks(time.perf_counter() - w0, tdist, dev)
         h2d = int(ht.numel() * ht.element_size() + hd.numel() * hd.element_size()
                   + htok.numel() * 4 + hseed.numel() * 8)
         d2h = int(sum(v.numel() * v.element_size() for v in res_host.values()))
-        e2e = {"value": B * world * ne / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_rows_per_s(B * ne, world, e2e_s), "unit": "rows/s",
+               "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ne}
 
     cpu = None
@@ -289,7 +305,7 @@ def run_ours(args):
         traffic = traffic_from_profile(args.workload)
         line = {
             "metric": METRIC,
-            "value": B * world * args.steps / (ms * 1e-3),
+            "value": job_rows_per_s(B * args.steps, world, ms * 1e-3),
             "unit": "rows/s",
             "n_gpus": world,
             "steps": args.steps,
