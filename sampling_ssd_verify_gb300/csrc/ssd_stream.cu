@@ -177,9 +177,10 @@ template <int TOPK>
 struct WarpList {
   float lv, cv;
   int li, ci;
-  int R;  // entries the row needs (F_j + 1 <= TOPK); the cut is entry R - 1
+  float hv;  // the head (best entry), known to all lanes
+  int R;     // entries the row needs (F_j + 1 <= TOPK); the cut is entry R - 1
   __device__ __forceinline__ void reset(int need) {
-    lv = cv = kNegInf;
+    lv = cv = hv = kNegInf;
     li = ci = 0x7fffffff;
     R = need;
   }
@@ -192,6 +193,7 @@ struct WarpList {
     const bool before = lane < R && cand_before(lv, li, v, i);
     const int pos = __popc(__ballot_sync(0xffffffffu, before));
     if (pos >= R) return;  // warp-uniform
+    if (pos == 0) hv = v;
     const float upv = __shfl_up_sync(0xffffffffu, lv, 1);
     const int upi = __shfl_up_sync(0xffffffffu, li, 1);
     if (lane > pos && lane < R) {
@@ -536,6 +538,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   // ordered float.  Piece numbers only increase within a CTA, so a value of
   // another piece is never mistaken for the current piece's.
   __shared__ unsigned long long s_cut;
+  // Each consumer warp's list head, (piece << 32) | ordered float: the heads
+  // of one piece are distinct logits of its row, so the R-th largest of them
+  // is a lower bound on the row's R-th best.
+  __shared__ unsigned long long s_head[kConsumerWarps];
   __shared__ PieceDesc s_pq[kPieceQueue];
 
   const int tid = threadIdx.x;
@@ -554,6 +560,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
     s_err = 0;
     s_cut = 0ull;
+    for (int i = 0; i < kConsumerWarps; ++i) s_head[i] = ~0ull;  // a tag no piece has
     fence_barrier_init();
   }
   __syncthreads();
@@ -739,7 +746,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       const uint32_t rc = __ldcg(p.row_cut + row);
       if (rc != 0u) ccut = unord_float(rc);
     }
-    float published = kNegInf;  // this warp's last published cut
+    float published = kNegInf;   // this warp's last published cut
+    float hpublished = kNegInf;  // and list head
     for (int64_t u = pu0, un = 0; u < pu1; u = un) {
       un = min(u + ups, pu1);
       const Stage st = stage_of<DT>(rg, p.V, u, un);
@@ -821,10 +829,31 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // below the largest cut of the CTA's warps (for this row) can enter
         // the row's top list.  A warp publishes its cut only when it rose
         // (cv is warp-uniform); every lane then reads the CTA-wide value.
+        const unsigned long long tag = (unsigned long long)(uint32_t)piece << 32;
         if (wl.cv != kNegInf && wl.cv > published) {
-          if (lane == 0)
-            atomicMax(&s_cut, ((unsigned long long)(uint32_t)piece << 32) | ord_float(wl.cv));
+          if (lane == 0) atomicMax(&s_cut, tag | ord_float(wl.cv));
           published = wl.cv;
+        }
+        if (wl.hv > hpublished) {
+          // A new head: publish it, then raise the cut to the R-th largest
+          // of this piece's heads (R distinct logits of the row reach it).
+          hpublished = wl.hv;
+          if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(&s_head[warp]) =
+              tag | ord_float(wl.hv);
+          __syncwarp();
+          const unsigned long long hw =
+              lane < kConsumerWarps ? *reinterpret_cast<volatile unsigned long long*>(&s_head[lane])
+                                    : ~0ull;
+          const float h = (hw >> 32) == (uint32_t)piece ? unord_float((uint32_t)hw) : kNegInf;
+          int rank = 0;
+#pragma unroll
+          for (int j = 0; j < kConsumerWarps; ++j) {
+            const float o = __shfl_sync(0xffffffffu, h, j);
+            rank += (o > h || (o == h && j < lane)) ? 1 : 0;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, lane < kConsumerWarps && rank == wl.R - 1);
+          const float hr = hit ? __shfl_sync(0xffffffffu, h, __ffs(hit) - 1) : kNegInf;
+          if (lane == 0 && hr != kNegInf) atomicMax(&s_cut, tag | ord_float(hr));
         }
         __syncwarp();
         const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(&s_cut);
