@@ -269,11 +269,29 @@ template <int TOPK>
 template <int DT, int NV>
 __device__ __forceinline__ void WarpList<TOPK>::offer(const uint4* raw, const float* vq, float vm,
                                                       int idx0, int kstride, float ccut) {
-  constexpr int VEC = Elem<DT>::kVec;
-  if (cv == kNegInf && NV * VEC * 32 >= R) ccut = fmaxf(ccut, boot_bound(vm));
   const bool anyq = vm != kNegInf && vm >= cv && vm >= ccut;
   if (!__any_sync(0xffffffffu, anyq)) return;
   offer_rare<DT, NV>(raw, vq, idx0, kstride, ccut, anyq);
+}
+
+// The R-th largest list head of piece `piece` on the CTA's board (one entry
+// per consumer warp, (piece << 32) | ordered float), or -inf when fewer than
+// R warps have published one.  Called by all 32 lanes.
+__device__ __forceinline__ float heads_cut(const unsigned long long* board, uint32_t piece,
+                                           int R) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long hw =
+      lane < kConsumerWarps ? *reinterpret_cast<const volatile unsigned long long*>(&board[lane])
+                            : ~0ull;
+  const float h = (hw >> 32) == piece ? unord_float((uint32_t)hw) : kNegInf;
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < kConsumerWarps; ++j) {
+    const float o = __shfl_sync(0xffffffffu, h, j);
+    rank += (o > h || (o == h && j < lane)) ? 1 : 0;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < kConsumerWarps && rank == R - 1);
+  return hit ? __shfl_sync(0xffffffffu, h, __ffs(hit) - 1) : kNegInf;
 }
 
 // Fold one stored partial into a lane's accumulator (row merges).
@@ -748,6 +766,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
     float published = kNegInf;   // this warp's last published cut
     float hpublished = kNegInf;  // and list head
+    bool booted = false;         // the piece's first full stage is done
+    const unsigned long long tag = (unsigned long long)(uint32_t)piece << 32;
     for (int64_t u = pu0, un = 0; u < pu1; u = un) {
       un = min(u + ups, pu1);
       const Stage st = stage_of<DT>(rg, p.V, u, un);
@@ -779,8 +799,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 #pragma unroll
         for (int q = 1; q < kVpt; ++q) vm = fmaxf(vm, vq[q]);
         a.take<N>(x, vm, c);
-        if (TOPK > 0 && top)
+        if (TOPK > 0 && top) {
+          if (!booted) {
+            // First full stage of the piece: bound the row's R-th best by the
+            // R-th largest lane maximum, and publish the warp's maximum as
+            // its head at once, so that warps that reach this stage later
+            // start from the R-th largest head already published.
+            booted = true;
+            const float bm = unord_float(__reduce_max_sync(0xffffffffu, ord_float(vm)));
+            if (lane == 0)
+              *reinterpret_cast<volatile unsigned long long*>(&s_head[warp]) = tag | ord_float(bm);
+            hpublished = bm;
+            __syncwarp();
+            ccut = fmaxf(ccut, fmaxf(wl.boot_bound(vm), heads_cut(s_head, (uint32_t)piece, wl.R)));
+          }
           wl.template offer<DT, kVpt>(raw, vq, vm, ei0 + tid * VEC, kConsumers * VEC, ccut);
+        }
       } else {
         // partial stage: warp-strided vectors so that every lane takes part
         for (int v0 = warp * 32; v0 < nvec; v0 += kConsumers) {
@@ -829,7 +863,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // below the largest cut of the CTA's warps (for this row) can enter
         // the row's top list.  A warp publishes its cut only when it rose
         // (cv is warp-uniform); every lane then reads the CTA-wide value.
-        const unsigned long long tag = (unsigned long long)(uint32_t)piece << 32;
         if (wl.cv != kNegInf && wl.cv > published) {
           if (lane == 0) atomicMax(&s_cut, tag | ord_float(wl.cv));
           published = wl.cv;
@@ -841,18 +874,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(&s_head[warp]) =
               tag | ord_float(wl.hv);
           __syncwarp();
-          const unsigned long long hw =
-              lane < kConsumerWarps ? *reinterpret_cast<volatile unsigned long long*>(&s_head[lane])
-                                    : ~0ull;
-          const float h = (hw >> 32) == (uint32_t)piece ? unord_float((uint32_t)hw) : kNegInf;
-          int rank = 0;
-#pragma unroll
-          for (int j = 0; j < kConsumerWarps; ++j) {
-            const float o = __shfl_sync(0xffffffffu, h, j);
-            rank += (o > h || (o == h && j < lane)) ? 1 : 0;
-          }
-          const unsigned hit = __ballot_sync(0xffffffffu, lane < kConsumerWarps && rank == wl.R - 1);
-          const float hr = hit ? __shfl_sync(0xffffffffu, h, __ffs(hit) - 1) : kNegInf;
+          const float hr = heads_cut(s_head, (uint32_t)piece, wl.R);
           if (lane == 0 && hr != kNegInf) atomicMax(&s_cut, tag | ord_float(hr));
         }
         __syncwarp();
