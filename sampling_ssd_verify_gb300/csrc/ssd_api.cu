@@ -54,6 +54,35 @@ ssd_status cuda_status(cudaError_t e) {
   return SSD_ERR_CUDA;
 }
 
+// Chunks per row of the streaming pass.  CTAs take chunks from a global
+// counter, so a CTA that meets costlier rows (more top-list insertions)
+// takes fewer.  Whole rows when there are at least two per CTA (a row split
+// over CTAs costs a partial merge and restarts its top-list pruning);
+// otherwise rows are cut into up to kMaxChunks equal non-empty chunks, about
+// four per CTA in all.  The launch and the workspace size both use it.
+int64_t stream_grid0() {
+  int sms = num_sms();
+  if (sms <= 0) sms = 1;
+  return std::min<int64_t>(sms, kMaxGrid);
+}
+
+int stream_chunk_len(int64_t NR, int upr) {
+  const int64_t grid0 = stream_grid0();
+  int64_t nch = 1;
+  if (NR < 2 * grid0) {
+    nch = (4 * grid0 + NR - 1) / NR;
+    nch = std::max<int64_t>(1, std::min<int64_t>({nch, (int64_t)kMaxChunks, (int64_t)upr}));
+  }
+  return (int)((upr + nch - 1) / nch);
+}
+
+int stream_chunks_per_row(int64_t NR, int upr) {
+  const int clen = stream_chunk_len(NR, upr);
+  return (upr + clen - 1) / clen;
+}
+
+int units_per_row(int V) { return (V + kUnitA - 1) / kUnitA; }
+
 struct Common {
   StreamParams sp;
   CdfParams cp;
@@ -65,7 +94,8 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
                  int nt, int nd, int V, float T, void* workspace, size_t ws_bytes,
                  cudaStream_t stream, Common& cm, WsLayout& L) {
   const int rpg = nt + nd;
-  L = ws_layout(groups, rpg, V);
+  L = ws_layout(groups, rpg, V,
+                stream_chunks_per_row((int64_t)groups * rpg, units_per_row(V)));
   if (workspace == nullptr || ((uintptr_t)workspace & 255) != 0 || ws_bytes < L.total)
     return SSD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -86,7 +116,7 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.nd = nd;
   p.rpg = rpg;
   p.NR = L.NR;
-  p.upr = (V + kUnitA - 1) / kUnitA;
+  p.upr = units_per_row(V);
   p.total_units = L.NR * p.upr;
   p.c = (float)(1.4426950408889634 / (double)T);  // log2(e) / T
   p.row_cnt = cnt;
@@ -134,24 +164,11 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   return SSD_OK;
 }
 
-// Chunks of the streaming pass.  CTAs take chunks from a global counter, so
-// a CTA that meets costlier rows (more top-list insertions) takes fewer.
-// Whole rows when there are at least two per CTA (a row split over CTAs
-// costs a partial merge and restarts its top-list pruning); otherwise rows
-// are cut into up to kMaxChunks equal chunks, about four per CTA in all.
 ssd_status run_stream(StreamParams& p, int dtype, int topk, cudaStream_t s) {
-  int sms = num_sms();
-  if (sms <= 0) sms = 1;
-  const int64_t grid0 = std::min<int64_t>(sms, kMaxGrid);
-  int64_t nch = 1;
-  if (p.NR < 2 * grid0) {
-    nch = (4 * grid0 + p.NR - 1) / p.NR;
-    nch = std::max<int64_t>(1, std::min<int64_t>({nch, (int64_t)kMaxChunks, (int64_t)p.upr}));
-  }
-  p.clen = (int)((p.upr + nch - 1) / nch);
-  p.nch = (p.upr + p.clen - 1) / p.clen;  // every chunk non-empty
+  p.clen = stream_chunk_len(p.NR, p.upr);
+  p.nch = (p.upr + p.clen - 1) / p.clen;
   p.nchunks = p.NR * p.nch;
-  const int grid = (int)std::min<int64_t>(grid0, p.nchunks);
+  const int grid = (int)std::min<int64_t>(stream_grid0(), p.nchunks);
   return cuda_status(launch_stream(p, dtype, topk, grid, s));
 }
 
@@ -224,17 +241,18 @@ ssd_status ssd_fanout(int K, int budget, double a, double r, int32_t* F_out) {
 size_t ssd_verify_workspace_size(int B, int K, int Kq, int V) {
   if (B < 1 || K < 1 || K > SSD_MAX_K || (Kq != K && Kq != K + 1) || V < 2 || V > SSD_MAX_V)
     return 0;
-  return ws_layout(B, K + 1 + Kq, V).total;
+  return ws_layout(B, K + 1 + Kq, V,
+                   stream_chunks_per_row((int64_t)B * (K + 1 + Kq), units_per_row(V))).total;
 }
 
 size_t ssd_topf_workspace_size(int B, int Kq, int V) {
   if (B < 1 || Kq < 1 || Kq > SSD_MAX_K + 1 || V < 2 || V > SSD_MAX_V) return 0;
-  return ws_layout(B, Kq, V).total;
+  return ws_layout(B, Kq, V, stream_chunks_per_row((int64_t)B * Kq, units_per_row(V))).total;
 }
 
 size_t ssd_saguaro_workspace_size(int R, int V) {
   if (R < 1 || V < 2 || V > SSD_MAX_V) return 0;
-  return ws_layout(R, 1, V).total;
+  return ws_layout(R, 1, V, stream_chunks_per_row((int64_t)R, units_per_row(V))).total;
 }
 
 ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,

@@ -156,7 +156,9 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-inline WsLayout ws_layout(int groups, int rpg, int V) {
+// nch: chunks per row of the streaming pass; split rows (nch > 1) need one
+// partial slot per chunk.
+inline WsLayout ws_layout(int groups, int rpg, int V, int nch) {
   WsLayout L;
   L.groups = groups;
   L.NR = (int64_t)groups * rpg;
@@ -168,7 +170,8 @@ inline WsLayout ws_layout(int groups, int rpg, int V) {
   L.ctr_off = (ncnt * sizeof(int) + 7) & ~(size_t)7;
   L.cnt_bytes = align256(L.ctr_off + 2 * sizeof(unsigned long long));  // stream, CDF
   L.part_off = L.cnt_bytes;
-  L.rowres_off = L.part_off + align256((size_t)L.NR * kMaxChunks * sizeof(RowPartial));
+  const size_t slots = nch > 1 ? (size_t)L.NR * nch : 1;
+  L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));
   L.gp_off = L.rowres_off + align256((size_t)L.NR * sizeof(RowResult));
   L.sub_off = L.gp_off + align256((size_t)groups * sizeof(GroupParams));
   L.dbg_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));
