@@ -52,6 +52,15 @@ struct Stage {
   uintptr_t b0, a0, a1;
 };
 
+// What the consumer warps need of a stage, written by the producer next to
+// the stage and published by the same mbarrier arrival: the aligned vectors
+// in shared memory (nvec, holding elements ei0 ...), and for the unaligned
+// head and tail the element range [e0, e1) at global address b0.
+struct StageDesc {
+  int nvec, ei0, e0, e1;
+  uintptr_t b0;
+};
+
 template <int DT>
 __device__ __forceinline__ const void* tensor_of(const StreamParams& p, int64_t row,
                                                  int64_t& trow, bool& is_t) {
@@ -130,6 +139,16 @@ struct Acc {
   }
 };
 
+// Two floats as one 64-bit register pair, for the packed f32x2 instructions.
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
 // Softmax accumulator of one consumer thread: running maximum m, its scaled
 // offset mc = fl(m*c) and the compensated sum (hi, lo) of 2^(z*c - mc).
 struct SAcc {
@@ -152,18 +171,44 @@ struct SAcc {
     lo = (t - hi) - y;
     hi = t;
   }
-  // n logits (all finite, or -inf padding) whose maximum is vm.
+  // n logits (all finite, or -inf padding) whose maximum is vm.  For n a
+  // multiple of 4 the exponent arguments and the pairwise tree sum use the
+  // packed f32x2 FMA / add (the same roundings, in the same order).
   template <int N>
   __device__ __forceinline__ void take(const float* x, float vm, float c) {
     if (vm > m) raise_max(vm, c);
     float e[N];
+    if constexpr (N % 4 == 0) {
+      const unsigned long long cc = pack2(c, c), mm = pack2(-mc, -mc);
 #pragma unroll
-    for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(x[k], c, -mc));
+      for (int k = 0; k < N; k += 2) {
+        unsigned long long d;
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(x[k], x[k + 1])), "l"(cc),
+            "l"(mm));
+        float a0, a1;
+        unpack2(d, a0, a1);
+        e[k] = ex2(a0);
+        e[k + 1] = ex2(a1);
+      }
 #pragma unroll
-    for (int w = N / 2; w > 0; w >>= 1)
+      for (int w = N / 2; w > 1; w >>= 1)
 #pragma unroll
-      for (int k = 0; k < w; ++k) e[k] += e[k + w];
-    if (N % 2 == 1 && N > 1) e[0] += e[N - 1];
+        for (int k = 0; k < w; k += 2) {
+          unsigned long long t;
+          asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(pack2(e[k], e[k + 1])),
+              "l"(pack2(e[k + w], e[k + w + 1])));
+          unpack2(t, e[k], e[k + 1]);
+        }
+      e[0] += e[1];
+    } else {
+#pragma unroll
+      for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(x[k], c, -mc));
+#pragma unroll
+      for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) e[k] += e[k + w];
+      if (N % 2 == 1 && N > 1) e[0] += e[N - 1];
+    }
     add(e[0]);
   }
 };
@@ -561,6 +606,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   // is a lower bound on the row's R-th best.
   __shared__ unsigned long long s_head[kConsumerWarps];
   __shared__ PieceDesc s_pq[kPieceQueue];
+  __shared__ StageDesc s_sd[kStagesA];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -617,6 +663,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           const Stage st = stage_of<DT>(rg, p.V, u, un);
           const int slot = n % kStagesA;
           if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+          StageDesc& sd = s_sd[slot];
+          sd.nvec = (int)((st.a1 - st.a0) >> 4);
+          sd.ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
+          sd.e0 = st.e0;
+          sd.e1 = st.e1;
+          sd.b0 = st.b0;
           const uint32_t bytes = (uint32_t)(st.a1 - st.a0);
           const bool tsrc = rg.is_t;
           if (bytes > 0 && !s_err &&
@@ -770,11 +822,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const unsigned long long tag = (unsigned long long)(uint32_t)piece << 32;
     for (int64_t u = pu0, un = 0; u < pu1; u = un) {
       un = min(u + ups, pu1);
-      const Stage st = stage_of<DT>(rg, p.V, u, un);
       const int slot = n % kStagesA;
       if (u != pu0) mbar_wait(full + slot, (n / kStagesA) & 1, &s_err, p.status);
-      const int nvec = (int)((st.a1 - st.a0) >> 4);
-      const int ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
+      const int nvec = s_sd[slot].nvec;
+      const int ei0 = s_sd[slot].ei0;
       const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
       constexpr int kVecs = kStageBytes / 16;
       constexpr int kVpt = kVecs / kConsumers;
@@ -835,10 +886,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
       }
       // unaligned head / tail elements (fewer than 32) by warp 0, from global memory
-      const int hc = nvec > 0 ? (int)((st.a0 - st.b0) / Elem<DT>::kSize) : st.e1 - st.e0;
-      const int ei1 = ei0 + nvec * VEC;
-      const int tc = nvec > 0 ? st.e1 - ei1 : 0;
       if (warp == 0) {
+        const StageDesc st = s_sd[slot];
+        const int hc = nvec > 0 ? ei0 - st.e0 : st.e1 - st.e0;
+        const int ei1 = ei0 + nvec * VEC;
+        const int tc = nvec > 0 ? st.e1 - ei1 : 0;
         for (int f0 = 0; f0 < hc + tc; f0 += 32) {
           const int f = f0 + lane;
           float x = kNegInf;
