@@ -671,6 +671,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           sd.b0 = st.b0;
           const uint32_t bytes = (uint32_t)(st.a1 - st.a0);
           const bool tsrc = rg.is_t;
+          (void)tsrc;  // read by the bounds-checked build only
           if (bytes > 0 && !s_err &&
               SSD_CHK(in_range(st.a0, st.a1, tsrc ? p.t_lo : p.d_lo, tsrc ? p.t_hi : p.d_hi),
                       p.dbg, 1, st.a0, st.a1)) {
@@ -782,10 +783,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   SAcc a;
   WarpList<(TOPK > 0 ? TOPK : 1)> wl;
   constexpr int VEC = Elem<DT>::kVec;
-  int n = 0;
+  int slot = 0;         // ring stage of the next stage
+  uint32_t phase = 0;   // its mbarrier phase parity
   for (int piece = 0;; ++piece) {
     // the piece's first stage (or the end marker) publishes its chunk
-    bool ok = mbar_wait(full + (n % kStagesA), (n / kStagesA) & 1, &s_err, p.status);
+    bool ok = mbar_wait(full + slot, phase, &s_err, p.status);
     const volatile PieceDesc& d = s_pq[piece % kPieceQueue];
     const long long chunk = ok ? d.chunk : -1ll;
     const int ps = piece % kPieceSlots;
@@ -806,7 +808,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int jr = d.jr;
     const bool is_t = jr < p.nt;
     const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
-    const RowGeom rg{d.rp, row * p.upr, is_t};
     a.reset();
     wl.reset(top ? p.F[jr - p.nt] + 1 : 1);
     // pruning bound for this row's top list: what earlier chunks of the row
@@ -820,10 +821,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     float hpublished = kNegInf;  // and list head
     bool booted = false;         // the piece's first full stage is done
     const unsigned long long tag = (unsigned long long)(uint32_t)piece << 32;
-    for (int64_t u = pu0, un = 0; u < pu1; u = un) {
-      un = min(u + ups, pu1);
-      const int slot = n % kStagesA;
-      if (u != pu0) mbar_wait(full + slot, (n / kStagesA) & 1, &s_err, p.status);
+    const int nst = (int)((pu1 - pu0 + ups - 1) / ups);  // stages of the piece
+    for (int s = 0; s < nst; ++s) {
+      if (s != 0) mbar_wait(full + slot, phase, &s_err, p.status);
       const int nvec = s_sd[slot].nvec;
       const int ei0 = s_sd[slot].ei0;
       const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
@@ -909,7 +909,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + slot);
-      ++n;
+      if (++slot == kStagesA) {
+        slot = 0;
+        phase ^= 1u;
+      }
       if (TOPK > 0 && top) {
         // The warp holds R candidates >= its cut cv, so no logit strictly
         // below the largest cut of the CTA's warps (for this row) can enter
