@@ -173,7 +173,7 @@ ssd_status run_stream(StreamParams& p, int dtype, int topk, cudaStream_t s) {
 }
 
 // Chunks of the CDF pass: about four per CTA in all, at most four pipeline
-// stages of kUnitsPerStageB units each.
+// stages of kUnitsPerStageB units each, taken in waves of groups.
 ssd_status run_cdf(CdfParams& q, int dtype, cudaStream_t s) {
   int sms = num_sms();
   if (sms <= 0) sms = 1;
@@ -183,6 +183,13 @@ ssd_status run_cdf(CdfParams& q, int dtype, cudaStream_t s) {
   q.cu = (int)cu;
   q.cpg = (q.nsub + q.cu - 1) / q.cu;
   q.nchunks = (int64_t)q.groups * q.cpg;
+  // Waves of about two chunks per CTA, so that a wave's groups are completed
+  // (and drawn) while the next wave streams -- when there are at least three
+  // such waves; otherwise one wave (the draws then come last, spread over
+  // all CTAs, which is shorter than a small last wave's).
+  q.wave = q.groups;
+  if (q.nchunks >= 6 * grid0)
+    q.wave = (int)std::max<int64_t>(1, (2 * grid0 + q.cpg - 1) / q.cpg);
   const int grid = (int)std::min<int64_t>(grid0, q.nchunks);
   return cuda_status(launch_cdf(q, dtype, grid, s));
 }

@@ -514,8 +514,10 @@ __device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupPa
 // their bulk copies, and kDrawWarps draw warps (chunk p of the CTA to warp
 // p mod kDrawWarps) count finished chunks into their group's arrival counter
 // and run the draw of the groups they complete, so the consumer warps never
-// wait for a draw.  Chunks go in the order (chunk of group, group): a group
-// is completed by its last chunk, and the draws spread over the CTAs.
+// wait for a draw.  Chunks go in waves of groups, in the order (chunk of
+// group, group) within a wave: a group is completed by its last chunk, the
+// draws of a wave spread over the CTAs and overlap the next wave's
+// streaming.
 constexpr int kCdfProducer = kConsumerWarps;
 constexpr int kCdfDrawWarp = kConsumerWarps + 1;  // the first draw warp
 constexpr int kDrawWarps = 2;
@@ -576,8 +578,15 @@ __global__ void __launch_bounds__(kCdfThreads, 1) cdf_kernel(const __grid_consta
         CdfDesc& d = s_q[piece % kCdfQueue];
         d.chunk = c;
         if (c >= 0) {
-          const int kc = (int)(c / p.groups);
-          const int64_t g = c - (int64_t)kc * p.groups;
+          // wave of `wave` groups (the last one may be smaller), then
+          // (chunk of group, group) within it
+          const int64_t per = (int64_t)p.wave * p.cpg;
+          const int64_t w = c / per;
+          const int64_t r = c - w * per;
+          const int64_t g0 = w * p.wave;
+          const int64_t gw = min((int64_t)p.wave, (int64_t)p.groups - g0);
+          const int kc = (int)(r / gw);
+          const int64_t g = g0 + (r - (int64_t)kc * gw);
           if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) d.chunk = -1;
           d.g = g;
           d.u0 = kc * p.cu;

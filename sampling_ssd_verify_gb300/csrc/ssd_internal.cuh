@@ -120,9 +120,9 @@ struct CdfParams {
   int groups, V, nsub;
   int64_t total_units;
   // Each group's nsub units are cut into cpg chunks of cu units (the last one
-  // shorter); CTAs take chunks in the order (chunk of group, group) from a
-  // global counter.
-  int cu, cpg;
+  // shorter).  CTAs take chunks from a global counter in waves of `wave`
+  // groups, in the order (chunk of group, group) within a wave.
+  int cu, cpg, wave;
   int64_t nchunks;
   unsigned long long* chunk_ctr;
   float c;
