@@ -24,7 +24,9 @@
  *     *_workspace_size() call.  The first bytes of the workspace (counters)
  *     are cleared on the stream at the start of every call, so a workspace
  *     needs no initialisation and may be reused by any entry point, but two
- *     calls that run concurrently must not share one.
+ *     calls that run concurrently must not share one.  Sizes depend on the
+ *     current device's SM count (small batches split rows over more CTAs):
+ *     query them with the device current that the call will run on.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream).  The library keeps no global state, so
  *     calls are thread-safe.
