@@ -92,6 +92,31 @@ __device__ __forceinline__ float weight(const GroupParams& gp, float c, int y, f
   }
 }
 
+// The weights of 16 consecutive tokens y0 .. y0+15 (0 from e1 on), with one
+// dispatch on the kind of draw for the whole run.
+template <int KIND, bool HAS_S>
+__device__ __forceinline__ void weights16_k(const GroupParams& gp, float c, int y0, int e1,
+                                            const float* zt, const float* zd, float* w) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    w[k] = y0 + k < e1 ? weight_k<KIND, HAS_S>(gp, c, y0 + k, zt[k], zd[k]) : 0.f;
+}
+
+__device__ __forceinline__ void weights16(const GroupParams& gp, float c, int y0, int e1,
+                                          const float* zt, const float* zd, float* w) {
+  const bool has_s = gp.theta != INFINITY;
+  switch (kind_of(gp)) {
+    case kTarget: weights16_k<kTarget, false>(gp, c, y0, e1, zt, zd, w); break;
+    case kSaguaro:
+      if (has_s) weights16_k<kSaguaro, true>(gp, c, y0, e1, zt, zd, w);
+      else weights16_k<kSaguaro, false>(gp, c, y0, e1, zt, zd, w);
+      break;
+    default:
+      if (has_s) weights16_k<kResidual, true>(gp, c, y0, e1, zt, zd, w);
+      else weights16_k<kResidual, false>(gp, c, y0, e1, zt, zd, w);
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ float weight_global(const CdfParams& p, const GroupParams& gp,
                                                const char* rt, const char* rd, int y) {
@@ -399,11 +424,10 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
     if (gp.use_t) load16<DT>(p, rt, true, y0, e1, zt);
     if (gp.use_d) load16<DT>(p, rd, false, y0, e1, zd);
     int lastpos = -1;
+    weights16(gp, p.c, y0, e1, zt, zd, w);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      w[k] = y0 + k < e1 ? weight(gp, p.c, y0 + k, zt[k], zd[k]) : 0.f;
+    for (int k = 0; k < 16; ++k)
       if (w[k] > 0.f) lastpos = y0 + k;
-    }
     const DF incl = df_warp_scan(df_sum16(w));
     const DF up = df_shfl_up(incl, 1);
     const DF excl = lane == 0 ? DF{0.f, 0.f} : up;
