@@ -58,8 +58,9 @@ ssd_status cuda_status(cudaError_t e) {
 // counter, so a CTA that meets costlier rows (more top-list insertions)
 // takes fewer.  Whole rows when there are at least two per CTA (a row split
 // over CTAs costs a partial merge and restarts its top-list pruning);
-// otherwise rows are cut into up to kMaxChunks equal non-empty chunks, about
-// four per CTA in all.  The launch and the workspace size both use it.
+// otherwise rows are cut into up to kMaxChunks equal non-empty chunks: about
+// four per CTA in all, or, for a few rows (a latency-bound pass), at most
+// one per CTA.  The launch and the workspace size both use it.
 int64_t stream_grid0() {
   int sms = num_sms();
   if (sms <= 0) sms = 1;
@@ -69,10 +70,13 @@ int64_t stream_grid0() {
 int stream_chunk_len(int64_t NR, int upr) {
   const int64_t grid0 = stream_grid0();
   int64_t nch = 1;
-  if (NR < 2 * grid0) {
+  if (2 * NR <= grid0) {
+    // a few rows (small batches): latency-bound, so one round of chunks
+    nch = grid0 / NR;
+  } else if (NR < 2 * grid0) {
     nch = (4 * grid0 + NR - 1) / NR;
-    nch = std::max<int64_t>(1, std::min<int64_t>({nch, (int64_t)kMaxChunks, (int64_t)upr}));
   }
+  nch = std::max<int64_t>(1, std::min<int64_t>({nch, (int64_t)kMaxChunks, (int64_t)upr}));
   return (int)((upr + nch - 1) / nch);
 }
 
@@ -178,7 +182,9 @@ ssd_status run_cdf(CdfParams& q, int dtype, cudaStream_t s) {
   int sms = num_sms();
   if (sms <= 0) sms = 1;
   const int64_t grid0 = std::min<int64_t>(sms, kMaxGrid);
-  int64_t cu = (q.total_units + 4 * grid0 - 1) / (4 * grid0);
+  // about four chunks per CTA; a small pass (latency-bound) takes one round
+  int64_t cu = q.total_units >= 8 * grid0 ? (q.total_units + 4 * grid0 - 1) / (4 * grid0)
+                                          : (q.total_units + grid0 - 1) / grid0;
   cu = std::max<int64_t>(1, std::min<int64_t>({cu, 4 * (int64_t)kUnitsPerStageB, (int64_t)q.nsub}));
   q.cu = (int)cu;
   q.cpg = (q.nsub + q.cu - 1) / q.cu;
