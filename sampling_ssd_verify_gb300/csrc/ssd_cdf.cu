@@ -596,7 +596,9 @@ __global__ void __launch_bounds__(kCdfThreads, 1) cdf_kernel(const __grid_consta
     // ---------------- producer ----------------
     if (lane == 0) {
       int n = 0;
-      unsigned long long next = atomicAdd(p.chunk_ctr, 1ull);
+      // the first round of chunks is static (chunk = CTA): a CTA's first
+      // copy does not wait behind every CTA's atomic on the counter
+      unsigned long long next = blockIdx.x;
       for (int piece = 0;; ++piece) {
         const long long c = next < (unsigned long long)p.nchunks ? (long long)next : -1ll;
         CdfDesc& d = s_q[piece % kCdfQueue];
@@ -624,7 +626,9 @@ __global__ void __launch_bounds__(kCdfThreads, 1) cdf_kernel(const __grid_consta
           ++n;
           break;
         }
-        next = atomicAdd(p.chunk_ctr, 1ull);  // the following chunk, fetched early
+        // the following chunk, fetched early (the counter hands out chunks
+        // after the static first round)
+        next = gridDim.x + atomicAdd(p.chunk_ctr, 1ull);
         const GroupParams gp = p.gp[d.g];
         d.gp = gp;  // published by the arrival on the chunk's first stage
         const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;

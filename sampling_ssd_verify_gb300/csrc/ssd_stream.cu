@@ -633,7 +633,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     // ---------------- producer ----------------
     if (lane == 0) {
       int n = 0;
-      unsigned long long next = atomicAdd(p.chunk_ctr, 1ull);
+      // the first round of chunks is static (chunk = CTA): a CTA's first
+      // copy does not wait behind every CTA's atomic on the counter
+      unsigned long long next = blockIdx.x;
       for (int piece = 0;; ++piece) {
         const long long c = next < (unsigned long long)p.nchunks ? (long long)next : -1ll;
         PieceDesc& d = s_pq[piece % kPieceQueue];
@@ -646,7 +648,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           ++n;
           break;
         }
-        next = atomicAdd(p.chunk_ctr, 1ull);  // the following chunk, fetched early
+        // the following chunk, fetched early (the counter hands out chunks
+        // after the static first round)
+        next = gridDim.x + atomicAdd(p.chunk_ctr, 1ull);
         int64_t row, pu0, pu1;
         int k;
         chunk_geom(p, c, row, k, pu0, pu1);
