@@ -241,19 +241,30 @@ def run_ours(args):
     ck = clocks.stop()
     ms = max_over_ranks(t0.elapsed_time(t1), tdist, dev)
     ms_step = ms / args.steps
-    verify_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_v]))
+    vts = [a.elapsed_time(b) for a, b in ev_v]
+    verify_ms = float(np.mean(vts))
+    verify_ms_median = float(np.median(vts))
     alg = w.algorithmic_bytes()
     hbm_peak, peak_kind = peaks()
     achieved = alg / (verify_ms * 1e-3) / 1e9
 
     # round statistics (untimed): acceptance, cache hit rate, all-rows-hit fraction
+    # alpha: accepted over attempted draft positions (a row that stops at n < K
+    # attempted n+1 of them); tail: the bonus draw's re-read, 2 rows (p and q')
+    # after a rejection, 1 row (p_K) after a full acceptance
     acc_sum, hits, all_hits, nr = 0.0, 0, 0, 100
+    att_sum, tail_rows = 0, 0
     for r in range(nr):
         step(50_000 + r)
-        acc_sum += float(out["accept_len"].float().mean().item())
+        al = out["accept_len"].cpu().numpy().astype(np.int64)
+        acc_sum += float(al.mean())
+        att_sum += int(np.minimum(al + 1, K).sum())
+        tail_rows += int(np.where(al < K, 2, 1).sum())
         hits += int((look["branch"] >= 0).sum().item())
         all_hits += int(look["all_hit"].item())
     h = hits / (nr * B)
+    alpha = acc_sum * B / max(att_sum, 1)
+    tail_bytes = tail_rows / nr * V * w.elem_bytes
 
     # end to end through the public API with host buffers
     e2e = None
@@ -324,13 +335,15 @@ def run_ours(args):
                              "inputs smaller than L2",
                        "positions_per_s": (K + 1) * B * world * args.steps / (ms * 1e-3),
                        "logits_gb_per_s": alg * world * args.steps / (ms * 1e-3) / 1e9,
-                       "accept_mean": acc_sum / nr, "hit_rate": h,
+                       "accept_mean": acc_sum / nr, "alpha_measured": alpha, "hit_rate": h,
                        "all_hit_fraction": all_hits / nr, "h_pow_B": h ** B,
                        "wall_s_timed": wall},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic,
                          "kernel": "ssd_verify (streaming pass + bonus draw)",
                          "algorithmic_bytes_per_launch": alg, "launch_ms": verify_ms,
+                         "launch_ms_median": verify_ms_median,
+                         "tail_bytes_per_launch": tail_bytes,
                          "peak_kind": peak_kind},
             "e2e": e2e,
             "gpu_launches": 5 * args.steps,
