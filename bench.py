@@ -346,7 +346,7 @@ def run_ours(args):
                          "tail_bytes_per_launch": tail_bytes,
                          "peak_kind": peak_kind},
             "e2e": e2e,
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": 4 * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

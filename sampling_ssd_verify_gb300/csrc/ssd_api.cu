@@ -1,7 +1,7 @@
 // ssd_api.cu -- the C-ABI entry points: argument validation, workspace
 // layout, launch configuration.  All arithmetic runs in the kernels of
-// ssd_stream.cu, ssd_cdf.cu and ssd_cache.cu; the one host computation is the
-// fan-out helper.
+// ssd_stream.cu (the streaming pass with the draws of ssd_cdf_dev.cuh) and
+// ssd_cache.cu; the one host computation is the fan-out helper.
 //
 // Sources: [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈";
 // [SD-7.3] "7.3 Speculative Decoding：投机采样加速".
@@ -126,6 +126,7 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.row_cnt = cnt;
   p.grp_cnt = cnt + L.NR;
   p.row_cut = reinterpret_cast<uint32_t*>(cnt + L.NR + 2 * groups);
+  p.grp_ready = cnt + 2 * L.NR + 2 * groups;
   p.chunk_ctr = reinterpret_cast<unsigned long long*>(ws + L.cnt_off + L.ctr_off);
   p.partials = reinterpret_cast<RowPartial*>(ws + L.part_off);
   p.rowres = reinterpret_cast<RowResult*>(ws + L.rowres_off);
@@ -159,7 +160,6 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   q.nt = nt;
   q.subsum = reinterpret_cast<float*>(ws + L.sub_off);
   q.cnt = cnt + L.NR + groups;
-  q.chunk_ctr = p.chunk_ctr + 1;
   q.t_lo = p.t_lo;
   q.t_hi = p.t_hi;
   q.d_lo = p.d_lo;
@@ -168,36 +168,38 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   return SSD_OK;
 }
 
-ssd_status run_stream(StreamParams& p, int dtype, int topk, cudaStream_t s) {
+// Chunking of the streaming pass and, when `draws`, of the draws that follow
+// it in the same launch; then the launch.
+//
+// Draws: units of kUnitB elements, fused_units_per_stage per ring stage, cut
+// into chunks of cu units -- about four per CTA in all, at most eight stages
+// each (a small pass, latency-bound, takes one round) -- and taken group by
+// group, the order in which the streaming pass completes the groups, so
+// that a chunk rarely waits for its group's parameters.
+ssd_status run_pass(Common& cm, int dtype, int topk, bool draws, cudaStream_t s) {
+  StreamParams& p = cm.sp;
+  CdfParams& q = cm.cp;
+  const int64_t grid0 = stream_grid0();
   p.clen = stream_chunk_len(p.NR, p.upr);
   p.nch = (p.upr + p.clen - 1) / p.clen;
   p.nchunks = p.NR * p.nch;
-  const int grid = (int)std::min<int64_t>(stream_grid0(), p.nchunks);
-  return cuda_status(launch_stream(p, dtype, topk, grid, s));
-}
-
-// Chunks of the CDF pass: about four per CTA in all, at most four pipeline
-// stages of kUnitsPerStageB units each, taken in waves of groups.
-ssd_status run_cdf(CdfParams& q, int dtype, cudaStream_t s) {
-  int sms = num_sms();
-  if (sms <= 0) sms = 1;
-  const int64_t grid0 = std::min<int64_t>(sms, kMaxGrid);
-  // about four chunks per CTA; a small pass (latency-bound) takes one round
-  int64_t cu = q.total_units >= 8 * grid0 ? (q.total_units + 4 * grid0 - 1) / (4 * grid0)
-                                          : (q.total_units + grid0 - 1) / grid0;
-  cu = std::max<int64_t>(1, std::min<int64_t>({cu, 4 * (int64_t)kUnitsPerStageB, (int64_t)q.nsub}));
-  q.cu = (int)cu;
-  q.cpg = (q.nsub + q.cu - 1) / q.cu;
-  q.nchunks = (int64_t)q.groups * q.cpg;
-  // Waves of about two chunks per CTA, so that a wave's groups are completed
-  // (and drawn) while the next wave streams -- when there are at least three
-  // such waves; otherwise one wave (the draws then come last, spread over
-  // all CTAs, which is shorter than a small last wave's).
-  q.wave = q.groups;
-  if (q.nchunks >= 6 * grid0)
-    q.wave = (int)std::max<int64_t>(1, (2 * grid0 + q.cpg - 1) / q.cpg);
-  const int grid = (int)std::min<int64_t>(grid0, q.nchunks);
-  return cuda_status(launch_cdf(q, dtype, grid, s));
+  q.nchunks = 0;
+  if (draws) {
+    const int ups = fused_units_per_stage(esize_of(dtype));
+    int64_t cu = q.total_units >= 8 * grid0 ? (q.total_units + 4 * grid0 - 1) / (4 * grid0)
+                                            : (q.total_units + grid0 - 1) / grid0;
+    cu = std::max<int64_t>(1, std::min<int64_t>({cu, 8 * (int64_t)ups, (int64_t)q.nsub}));
+    q.cu = (int)cu;
+    q.cpg = (q.nsub + q.cu - 1) / q.cu;
+    q.nchunks = (int64_t)q.groups * q.cpg;
+  } else {
+    p.grp_ready = nullptr;
+  }
+  VerifyParams vp;
+  vp.s = p;
+  vp.q = q;
+  const int grid = (int)std::min<int64_t>(grid0, p.nchunks + q.nchunks);
+  return cuda_status(launch_stream(vp, dtype, topk, grid, s));
 }
 
 int64_t capacity_of(size_t table_bytes) {
@@ -315,14 +317,12 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
   p.guess_q = guess_q;
   p.Fmax = Fmax;
   p.status = dev_status;
-  st = run_stream(p, target->dtype, need_top ? topk_for(maxF) : 0, s);
-  if (st != SSD_OK) return st;
   CdfParams& q = cm.cp;
   q.mode = kModeVerify;
   q.out_token = bonus;
   q.out_mass = resid_mass;
   q.status = dev_status;
-  return run_cdf(q, target->dtype, s);
+  return run_pass(cm, target->dtype, need_top ? topk_for(maxF) : 0, true, s);
 }
 
 ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T,
@@ -357,7 +357,7 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
   p.guess_q = guess_q;
   p.Fmax = Fmax;
   p.status = dev_status;
-  return run_stream(p, draft->dtype, maxF > 0 ? topk_for(maxF) : 0, s);
+  return run_pass(cm, draft->dtype, maxF > 0 ? topk_for(maxF) : 0, false, s);
 }
 
 ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, float C, int F,
@@ -383,8 +383,6 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
   p.jpos = j;
   p.mode = kModeSaguaro;
   p.status = dev_status;
-  st = run_stream(p, draft->dtype, need_top ? topk_for(F) : 0, s);
-  if (st != SSD_OK) return st;
   CdfParams& q = cm.cp;
   q.mode = kModeSaguaro;
   q.out_token = out_token;
@@ -392,7 +390,7 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
   q.out_guess = F > 0 ? out_guess : nullptr;
   q.F = F;
   q.status = dev_status;
-  return run_cdf(q, draft->dtype, s);
+  return run_pass(cm, draft->dtype, need_top ? topk_for(F) : 0, true, s);
 }
 
 size_t ssd_cache_bytes(int n_keys) {

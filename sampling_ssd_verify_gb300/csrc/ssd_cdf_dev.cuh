@@ -1,24 +1,21 @@
-// ssd_cdf.cu -- the inverse-CDF draw over one vocabulary row per group.
+// ssd_cdf_dev.cuh -- device code of the inverse-CDF draw, which the
+// streaming kernel (ssd_stream.cu) runs after the rows in the same launch.
 //
-// After the streaming pass every group (a verified sequence, or a Saguaro
-// branch row) has its draw parameters: the bonus weight
-//   w(y) = (p_k(y) - q'_k(y))^+   when a draft was rejected at k < K,
-//   w(y) = p_K(y)                 when every draft was accepted
-// ([SD-7.3] §7.3.3 for the residual, §7.3.2 for the all-accepted bonus), or
-// the Saguaro draft distribution w(y) = q'(y) for a continuation draw
-// ([SSD-note] §"Saguaro 优化二：Saguaro 采样").  The token drawn is the
-// smallest y with sum_{y'<=y} w(y') > u * Z, Z = sum_y w(y).
+// The bonus weight of a verified sequence is w(y) = (p_k(y) - q'_k(y))^+
+// after a rejection at k < K and w(y) = p_K(y) when every draft was accepted
+// ([SD-7.3] §7.3.3 for the residual, §7.3.2 for the all-accepted bonus); a
+// Saguaro continuation draws from w(y) = q'(y) ([SSD-note] §"Saguaro
+// 优化二：Saguaro 采样").  The token drawn is the smallest y with
+// sum_{y'<=y} w(y') > u * Z, Z = sum_y w(y).
 //
-// Work is split into 512-element units over (group, unit), and the units of
-// a group into chunks that persistent CTAs (one per SM) take from a global
-// counter.  A CTA streams a chunk of the one or two rows the group needs
-// through a bulk-copy ring, each consumer warp reduces one unit to its weight
-// sum, and the CTA that completes a group (atomic arrival counter) locates
-// the unit holding u*Z by a prefix over the unit sums and scans that unit in
-// vocabulary order.
+// Work is split into kUnitB-element units; the sum of the weights of each
+// unit is stored, and the chunk that completes a group runs its draw: the
+// unit holding u*Z by a prefix over the unit sums, then a vocabulary-order
+// scan of that unit.
 //
 // Sources: [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈";
 // [SD-7.3] "7.3 Speculative Decoding：投机采样加速".
+#pragma once
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -27,7 +24,6 @@
 #include "ssd_internal.cuh"
 
 namespace ssd {
-
 namespace {
 
 // One row half of a stage: where element y lives (shared memory or global).
@@ -38,10 +34,10 @@ struct Half {
 };
 
 template <int DT>
-__device__ __forceinline__ float fetch(const Half& h, int y, const CdfParams& p, bool is_t) {
+__device__ __forceinline__ float fetch(const Half& h, int y, const CdfParams& p, bool is_t,
+                                       int half) {
   if (y >= h.ei0 && y < h.ei1) {
-    if (!SSD_CHK((y - h.ei0) * Elem<DT>::kSize < kUnitsPerStageB * kUnitB * Elem<DT>::kSize,
-                 p.dbg, 24, y, h.ei0))
+    if (!SSD_CHK((y - h.ei0) * Elem<DT>::kSize < half, p.dbg, 24, y, h.ei0))
       return 0.f;
     return Elem<DT>::smem(h.sm, y - h.ei0);
   }
@@ -50,6 +46,18 @@ __device__ __forceinline__ float fetch(const Half& h, int y, const CdfParams& p,
                p.dbg, 22, y, (int64_t)(a - (uintptr_t)(is_t ? p.t_lo : p.d_lo))))
     return 0.f;
   return Elem<DT>::load(h.row, y);
+}
+
+// A group's draw parameters, read from L2: another CTA of the same launch
+// may have written them.
+__device__ __forceinline__ GroupParams load_gp(const GroupParams* src) {
+  static_assert(sizeof(GroupParams) % 8 == 0, "GroupParams is read as 8-byte words");
+  GroupParams gp;
+  const unsigned long long* a = reinterpret_cast<const unsigned long long*>(src);
+  unsigned long long* b = reinterpret_cast<unsigned long long*>(&gp);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(GroupParams) / 8); ++i) b[i] = __ldcg(a + i);
+  return gp;
 }
 
 // The draw weight of token y given its target logit zt and draft logit zd.
@@ -300,6 +308,7 @@ __device__ __forceinline__ void load16(const CdfParams& p, const char* r, bool i
     for (int k = 0; k < 16; ++k) {
       const int y = y0 + k;
       const uintptr_t ay = (uintptr_t)(r + (int64_t)y * ES);
+      (void)ay;  // read by the bounds-checked build only
       z[k] = (y < e1 && SSD_CHK(in_range(ay, ay + ES, is_t ? p.t_lo : p.d_lo,
                                          is_t ? p.t_hi : p.d_hi), p.dbg, 29, y, e1))
                  ? Elem<DT>::load(r, y) : 0.f;
@@ -334,7 +343,7 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
     }
   };
   load_round(0);  // in flight together with the group's parameters
-  const GroupParams gp = p.gp[g];
+  const GroupParams gp = load_gp(p.gp + g);
   const int esz = Elem<DT>::kSize;
   const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, esz) : nullptr;
   const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, esz) : nullptr;
@@ -474,16 +483,6 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   }
 }
 
-// Ring geometry of the CDF pass: a stage holds kUnitsPerStageB units of the
-// target row and of the draft row.
-template <int DT>
-struct CdfRing {
-  static constexpr int ES = Elem<DT>::kSize;
-  static constexpr int HALF = kUnitsPerStageB * kUnitB * ES;
-  static constexpr int STAGE = 2 * HALF;
-  static constexpr int NST = kRingBytesB / STAGE;
-};
-
 // Sum of the draw weights of one whole unit whose elements sit 16-byte
 // aligned in shared memory (vectorised fast path of one warp), specialised
 // per kind of draw.
@@ -533,276 +532,130 @@ __device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupPa
   }
 }
 
-// Warp roles: warps 0..kConsumerWarps-1 sum units (one unit per warp and
-// stage), warp kConsumerWarps takes chunks from the global counter and issues
-// their bulk copies, and kDrawWarps draw warps (chunk p of the CTA to warp
-// p mod kDrawWarps) count finished chunks into their group's arrival counter
-// and run the draw of the groups they complete, so the consumer warps never
-// wait for a draw.  Chunks go in waves of groups, in the order (chunk of
-// group, group) within a wave: a group is completed by its last chunk, the
-// draws of a wave spread over the CTAs and overlap the next wave's
-// streaming.
-constexpr int kCdfProducer = kConsumerWarps;
-constexpr int kCdfDrawWarp = kConsumerWarps + 1;  // the first draw warp
-constexpr int kDrawWarps = 2;
-constexpr int kCdfThreads = (kConsumerWarps + 1 + kDrawWarps) * 32;
-constexpr int kDrawSlots = 8;   // chunks the draw warps may lag behind
-static_assert(kDrawSlots % kDrawWarps == 0, "a slot belongs to one draw warp");
-constexpr int kCdfQueue = 32;   // chunk descriptors in flight
+// Chunk c of the draws: group g and its units [u0, u1), group by group.
+__device__ __forceinline__ void cdf_chunk_geom(const CdfParams& p, long long c, int64_t& g,
+                                               int& u0, int& u1) {
+  g = c / p.cpg;
+  u0 = (int)(c - g * p.cpg) * p.cu;
+  u1 = min(u0 + p.cu, p.nsub);
+}
 
-// A chunk as the producer hands it on (chunk -1: the end).
-struct CdfDesc {
-  long long chunk;
-  int64_t g;       // group
-  int u0, u1;      // units [u0, u1) of the group
-  GroupParams gp;  // the group's draw parameters
-};
-
+// Bulk copies of units [u, un) of a group's target row rt and draft row rd
+// (null: not part of the weight) into one stage: the target run at dst, the
+// draft run at dst + half, each from its first 16-byte boundary to its last;
+// completion is counted on `bar`.  One thread.
 template <int DT>
-__global__ void __launch_bounds__(kCdfThreads, 1) cdf_kernel(const __grid_constant__ CdfParams p) {
+__device__ __forceinline__ void cdf_issue_stage(const CdfParams& p, const char* rt,
+                                                const char* rd, int u, int un,
+                                                unsigned char* dst, int half, uint64_t* bar,
+                                                volatile int* s_err) {
   constexpr int ES = Elem<DT>::kSize;
-  constexpr int HALF = CdfRing<DT>::HALF;
-  constexpr int STAGE = CdfRing<DT>::STAGE;
-  constexpr int kStagesB = CdfRing<DT>::NST;
-  static_assert(kCdfQueue > kStagesB + 1 + kDrawSlots, "descriptor queue too short");
-  extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesB * STAGE);
-  uint64_t* empty = full + kStagesB;
-  uint64_t* cdone = empty + kStagesB;
-  uint64_t* cempty = cdone + kDrawSlots;
-  __shared__ int s_err;
-  __shared__ CdfDesc s_q[kCdfQueue];
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-
-  if (tid == 0) {
-    for (int i = 0; i < kStagesB; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(empty + i, kConsumerWarps);
-    }
-    for (int i = 0; i < kDrawSlots; ++i) {
-      mbar_init(cdone + i, kConsumerWarps);
-      mbar_init(cempty + i, 1);
-    }
-    s_err = 0;
-    fence_barrier_init();
+  const int e0 = u * kUnitB;
+  const int e1 = min(p.V, un * kUnitB);
+  uintptr_t a0[2] = {0, 0}, a1[2] = {0, 0};
+  uint32_t bytes = 0;
+  for (int h = 0; h < 2; ++h) {
+    const char* r = h == 0 ? rt : rd;
+    if (r == nullptr) continue;
+    const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
+    const uintptr_t b1 = (uintptr_t)(r + (int64_t)e1 * ES);
+    a0[h] = (b0 + 15) & ~(uintptr_t)15;
+    a1[h] = b1 & ~(uintptr_t)15;
+    if (a1[h] > a0[h]) bytes += (uint32_t)(a1[h] - a0[h]);
   }
-  __syncthreads();
+  bool srcok = true;
+  for (int h = 0; h < 2; ++h)
+    if (a1[h] > a0[h])
+      srcok &= SSD_CHK(in_range(a0[h], a1[h], h == 0 ? p.t_lo : p.d_lo, h == 0 ? p.t_hi : p.d_hi),
+                       p.dbg, 21, a0[h], h);
+  srcok &= SSD_CHK((un - u) * kUnitB * ES <= half, p.dbg, 28, un - u, half);
+  if (bytes > 0 && !*s_err && srcok) {
+    mbar_arrive_expect_tx(bar, bytes);
+    for (int h = 0; h < 2; ++h)
+      if (a1[h] > a0[h])
+        bulk_g2s(dst + h * half, reinterpret_cast<const void*>(a0[h]), (uint32_t)(a1[h] - a0[h]),
+                 bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
 
-  if (warp == kCdfProducer) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      int n = 0;
-      // the first round of chunks is static (chunk = CTA): a CTA's first
-      // copy does not wait behind every CTA's atomic on the counter
-      unsigned long long next = blockIdx.x;
-      for (int piece = 0;; ++piece) {
-        const long long c = next < (unsigned long long)p.nchunks ? (long long)next : -1ll;
-        CdfDesc& d = s_q[piece % kCdfQueue];
-        d.chunk = c;
-        if (c >= 0) {
-          // wave of `wave` groups (the last one may be smaller), then
-          // (chunk of group, group) within it
-          const int64_t per = (int64_t)p.wave * p.cpg;
-          const int64_t w = c / per;
-          const int64_t r = c - w * per;
-          const int64_t g0 = w * p.wave;
-          const int64_t gw = min((int64_t)p.wave, (int64_t)p.groups - g0);
-          const int kc = (int)(r / gw);
-          const int64_t g = g0 + (r - (int64_t)kc * gw);
-          if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) d.chunk = -1;
-          d.g = g;
-          d.u0 = kc * p.cu;
-          d.u1 = min(d.u0 + p.cu, p.nsub);
-        }
-        if (d.chunk < 0) {
-          // end marker: one stage without data
-          const int slot = n % kStagesB;
-          if (n >= kStagesB) mbar_wait(empty + slot, ((n / kStagesB) - 1) & 1, &s_err, p.status);
-          mbar_arrive(full + slot);
-          ++n;
-          break;
-        }
-        // the following chunk, fetched early (the counter hands out chunks
-        // after the static first round)
-        next = gridDim.x + atomicAdd(p.chunk_ctr, 1ull);
-        const GroupParams gp = p.gp[d.g];
-        d.gp = gp;  // published by the arrival on the chunk's first stage
-        const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;
-        const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, ES) : nullptr;
-        for (int u = d.u0, un = 0; u < d.u1; u = un) {
-          un = min(u + kUnitsPerStageB, d.u1);
-          const int e0 = u * kUnitB;
-          const int e1 = min(p.V, un * kUnitB);
-          const int slot = n % kStagesB;
-          if (n >= kStagesB) mbar_wait(empty + slot, ((n / kStagesB) - 1) & 1, &s_err, p.status);
-          uintptr_t a0[2] = {0, 0}, a1[2] = {0, 0};
-          uint32_t bytes = 0;
-          for (int h = 0; h < 2; ++h) {
-            const char* r = h == 0 ? rt : rd;
-            if (r == nullptr) continue;
-            const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
-            const uintptr_t b1 = (uintptr_t)(r + (int64_t)e1 * ES);
-            a0[h] = (b0 + 15) & ~(uintptr_t)15;
-            a1[h] = b1 & ~(uintptr_t)15;
-            if (a1[h] > a0[h]) bytes += (uint32_t)(a1[h] - a0[h]);
-          }
-          bool srcok = true;
-          for (int h = 0; h < 2; ++h)
-            if (a1[h] > a0[h])
-              srcok &= SSD_CHK(in_range(a0[h], a1[h], h == 0 ? p.t_lo : p.d_lo,
-                                        h == 0 ? p.t_hi : p.d_hi), p.dbg, 21, a0[h], h);
-          if (bytes > 0 && !s_err && srcok) {
-            mbar_arrive_expect_tx(full + slot, bytes);
-            for (int h = 0; h < 2; ++h)
-              if (a1[h] > a0[h])
-                bulk_g2s(ring + slot * STAGE + h * HALF, reinterpret_cast<const void*>(a0[h]),
-                         (uint32_t)(a1[h] - a0[h]), full + slot);
-          } else {
-            mbar_arrive(full + slot);
-          }
-          ++n;
-        }
+// The weight sums of units [u, un) of group g, staged by cdf_issue_stage at
+// `stage`: consumer warp `warp` takes unit u + warp, and its lane 0 stores
+// the sum.  Units whose elements are not all in shared memory, 16-byte
+// aligned (row ends, unaligned rows), read the missing ones from global
+// memory.
+template <int DT>
+__device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
+                                                  const GroupParams& gp, const char* rt,
+                                                  const char* rd, int u, int un,
+                                                  const unsigned char* stage, int half,
+                                                  int warp) {
+  constexpr int ES = Elem<DT>::kSize;
+  const int lane = threadIdx.x & 31;
+  const int uu = u + warp;
+  if (uu >= un) return;
+  const int e0 = u * kUnitB;
+  const int e1 = min(p.V, un * kUnitB);
+  Half ht, hd;
+  for (int h = 0; h < 2; ++h) {
+    Half& H = h == 0 ? ht : hd;
+    const char* r = h == 0 ? rt : rd;
+    H.row = r;
+    H.sm = reinterpret_cast<const char*>(stage + h * half);
+    H.ei0 = H.ei1 = e0;
+    if (r != nullptr) {
+      const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
+      const uintptr_t b1 = (uintptr_t)(r + (int64_t)e1 * ES);
+      const uintptr_t A0 = (b0 + 15) & ~(uintptr_t)15;
+      const uintptr_t A1 = b1 & ~(uintptr_t)15;
+      if (A1 > A0) {
+        H.ei0 = e0 + (int)((A0 - b0) / ES);
+        H.ei1 = H.ei0 + (int)((A1 - A0) / ES);
       }
-      // do not leave while copies into this CTA's shared memory are in flight
-      for (int q = max(0, n - kStagesB); q < n; ++q)
-        mbar_wait(full + (q % kStagesB), (q / kStagesB) & 1, &s_err, p.status);
     }
-    return;
   }
-
-  if (warp >= kCdfDrawWarp) {
-    // ---------------- draw: group arrival, then the draw ----------------
-    for (int piece = warp - kCdfDrawWarp;; piece += kDrawWarps) {
-      const int ds = piece % kDrawSlots;
-      if (!mbar_wait(cdone + ds, (piece / kDrawSlots) & 1, &s_err, p.status)) break;
-      const CdfDesc& d = s_q[piece % kCdfQueue];
-      const long long chunk = d.chunk;
-      const int64_t g = d.g;
-      const int nu = d.u1 - d.u0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cempty + ds);
-      if (chunk < 0) break;
-      // this chunk's unit sums are written: count them into the group
-      int last = 0;
-      if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(p.cnt + g, nu) + nu == p.nsub;
-        if (last) __threadfence();
+  const int ue0 = uu * kUnitB;
+  const int ue1 = min(ue0 + kUnitB, p.V);
+  constexpr int VEC = Elem<DT>::kVec;
+  bool fast = ue1 - ue0 == kUnitB;
+  if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
+  if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
+  float s = 0.f;
+  if (fast) {
+    s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
+  } else {
+    for (int m = 0; m < kUnitB / 32; ++m) {
+      const int y = ue0 + lane + 32 * m;
+      if (y < ue1) {
+        const float zt = gp.use_t ? fetch<DT>(ht, y, p, true, half) : 0.f;
+        const float zd = gp.use_d ? fetch<DT>(hd, y, p, false, half) : 0.f;
+        s += weight(gp, p.c, y, zt, zd);
       }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) group_draw<DT>(p, g);
     }
-    return;
   }
-
-  // ---------------- consumers ----------------
-  int n = 0;
-  for (int piece = 0;; ++piece) {
-    // the chunk's first stage (or the end marker) publishes its descriptor
-    const bool ok = mbar_wait(full + (n % kStagesB), (n / kStagesB) & 1, &s_err, p.status);
-    const CdfDesc& d = s_q[piece % kCdfQueue];
-    const long long chunk = ok ? d.chunk : -1ll;
-    if (chunk >= 0) {
-      const int64_t g = d.g;
-      const int u0 = d.u0, u1 = d.u1;
-      const GroupParams gp = d.gp;
-      const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : nullptr;
-      const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, ES) : nullptr;
-      for (int u = u0, un = 0; u < u1; u = un) {
-        un = min(u + kUnitsPerStageB, u1);
-        const int e0 = u * kUnitB;
-        const int e1 = min(p.V, un * kUnitB);
-        const int slot = n % kStagesB;
-        if (u != u0) mbar_wait(full + slot, (n / kStagesB) & 1, &s_err, p.status);
-        Half ht, hd;
-        for (int h = 0; h < 2; ++h) {
-          Half& H = h == 0 ? ht : hd;
-          const char* r = h == 0 ? rt : rd;
-          H.row = r;
-          H.sm = reinterpret_cast<const char*>(ring + slot * STAGE + h * HALF);
-          H.ei0 = H.ei1 = e0;
-          if (r != nullptr) {
-            const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
-            const uintptr_t b1 = (uintptr_t)(r + (int64_t)e1 * ES);
-            const uintptr_t A0 = (b0 + 15) & ~(uintptr_t)15;
-            const uintptr_t A1 = b1 & ~(uintptr_t)15;
-            if (A1 > A0) {
-              H.ei0 = e0 + (int)((A0 - b0) / ES);
-              H.ei1 = H.ei0 + (int)((A1 - A0) / ES);
-            }
-          }
-        }
-        const int uu = u + warp;
-        if (uu < un) {
-          const int ue0 = uu * kUnitB;
-          const int ue1 = min(ue0 + kUnitB, p.V);
-          constexpr int VEC = Elem<DT>::kVec;
-          bool fast = ue1 - ue0 == kUnitB;
-          if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
-          if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
-          float s = 0.f;
-          if (fast) {
-            s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
-          } else {
-            for (int m = 0; m < kUnitB / 32; ++m) {
-              const int y = ue0 + lane + 32 * m;
-              if (y < ue1) {
-                const float zt = gp.use_t ? fetch<DT>(ht, y, p, true) : 0.f;
-                const float zd = gp.use_d ? fetch<DT>(hd, y, p, false) : 0.f;
-                s += weight(gp, p.c, y, zt, zd);
-              }
-            }
-          }
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-          if (lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
-            p.subsum[g * p.nsub + uu] = s;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty + slot);
-        ++n;
-      }
-    }
-    // hand the finished chunk (or end markers for every draw warp) on
-    for (int q = piece; q < piece + (chunk < 0 ? kDrawWarps : 1); ++q) {
-      const int qs = q % kDrawSlots;
-      if (lane == 0 && q >= kDrawSlots)
-        mbar_wait(cempty + qs, ((q / kDrawSlots) - 1) & 1, &s_err, p.status);
-      // the producer wrote one end marker; the extra ones are marked here
-      if (q > piece && warp == 0 && lane == 0) s_q[q % kCdfQueue].chunk = -1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cdone + qs);
-    }
-    if (chunk < 0) break;
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
+    p.subsum[g * p.nsub + uu] = s;
+}
+
+// A finished chunk of group g (nu units, their sums stored): count it into
+// the group's arrivals; the warp whose chunk completes the group runs the
+// draw.  One warp.
+template <int DT>
+__device__ __forceinline__ void cdf_chunk_done(const CdfParams& p, int64_t g, int nu) {
+  const int lane = threadIdx.x & 31;
+  if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) return;
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();
+    last = atomicAdd(p.cnt + g, nu) + nu == p.nsub;
+    if (last) __threadfence();
   }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) group_draw<DT>(p, g);
 }
 
 }  // namespace
-
-int cdf_smem_bytes(int dtype) {
-  const int bars = 2 * kDrawSlots * (int)sizeof(uint64_t);
-  return dtype == SSD_BF16
-             ? CdfRing<0>::NST * CdfRing<0>::STAGE + 2 * CdfRing<0>::NST * (int)sizeof(uint64_t) + bars
-             : CdfRing<1>::NST * CdfRing<1>::STAGE + 2 * CdfRing<1>::NST * (int)sizeof(uint64_t) + bars;
-}
-
-cudaError_t launch_cdf(const CdfParams& p, int dtype, int grid, cudaStream_t s) {
-  const int smem = cdf_smem_bytes(dtype);
-  cudaError_t e;
-  if (dtype == SSD_BF16) {
-    e = cudaFuncSetAttribute(cdf_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    cdf_kernel<0><<<grid, kCdfThreads, smem, s>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(cdf_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    cdf_kernel<1><<<grid, kCdfThreads, smem, s>>>(p);
-  }
-  return cudaGetLastError();
-}
-
 }  // namespace ssd

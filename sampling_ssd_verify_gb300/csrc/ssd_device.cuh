@@ -88,6 +88,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// A flag another CTA of the launch sets once: release store / acquire load
+// at GPU scope.
+__device__ __forceinline__ void flag_release(int* f) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(1) : "memory");
+}
+__device__ __forceinline__ int flag_acquire(const int* f) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+
+// Wait (bounded, like mbar_wait) until the flag is set; false on a timeout
+// or when the CTA has already met an error.  One thread.
+__device__ __forceinline__ bool flag_wait(const int* f, volatile int* s_err, int32_t* status) {
+  if (flag_acquire(f)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (*s_err) return false;
+    __nanosleep(256);
+    if (flag_acquire(f)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *s_err = 1;
+      if (status) atomicOr(status, SSD_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

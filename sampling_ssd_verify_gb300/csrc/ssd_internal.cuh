@@ -22,8 +22,9 @@ constexpr int kUnitA = 1024;                        // elements per work unit, s
 constexpr int kStageBytes = 32768;                  // bytes per pipeline stage
 constexpr int kStagesA = 6;                         // ring depth, streaming pass
 constexpr int kUnitB = 512;                         // elements per unit, CDF pass
-constexpr int kUnitsPerStageB = kConsumerWarps;     // one unit per consumer warp
-constexpr int kRingBytesB = 196608;                // bulk-copy ring of the CDF pass
+// units of the draws per stage of the streaming ring (target and draft runs
+// of kStageBytes / 2 each)
+__host__ __device__ constexpr int fused_units_per_stage(int esize) { return kStageBytes / 2 / (kUnitB * esize); }
 constexpr int kMaxTopK = 16;                        // per-row candidate list (F + 1 <= 16)
 constexpr int kMaxGrid = 4096;                      // bound on CTAs of one launch
 constexpr int kMaxChunks = 16;                      // bound on chunks per row (streaming pass)
@@ -100,6 +101,7 @@ struct StreamParams {
   int Fmax;
   int* row_cnt;
   int* grp_cnt;
+  int* grp_ready;           // per group: 1 once its draw parameters are published
   RowPartial* partials;     // slot row * nch + chunk of row
   RowResult* rowres;
   GroupParams* gparams;
@@ -120,11 +122,9 @@ struct CdfParams {
   int groups, V, nsub;
   int64_t total_units;
   // Each group's nsub units are cut into cpg chunks of cu units (the last one
-  // shorter).  CTAs take chunks from a global counter in waves of `wave`
-  // groups, in the order (chunk of group, group) within a wave.
-  int cu, cpg, wave;
+  // shorter), taken group by group.
+  int cu, cpg;
   int64_t nchunks;
-  unsigned long long* chunk_ctr;
   float c;
   int mode;
   const GroupParams* gp;
@@ -145,10 +145,20 @@ struct CdfParams {
   unsigned long long* dbg;
 };
 
+// The streaming pass and the draws in one persistent launch: logical chunks
+// [0, s.nchunks) stream rows, [s.nchunks, s.nchunks + q.nchunks) are chunks
+// of the draws (none when q.nchunks is 0), all taken from the one counter
+// s.chunk_ctr.  A chunk of the draws waits until its group's
+// parameters are published (s.grp_ready), so the launch is cooperative.
+struct VerifyParams {
+  StreamParams s;
+  CdfParams q;
+};
+
 // ---- workspace layout ----------------------------------------------------------
 struct WsLayout {
   size_t cnt_off, cnt_bytes;       // counters (cleared each call)
-  size_t ctr_off;                  // chunk counters (streaming, CDF pass), within the counters
+  size_t ctr_off;                  // the chunk counter, within the counters
   size_t part_off, rowres_off, gp_off, sub_off, dbg_off, total;
   int64_t NR;
   int groups, nsub;
@@ -164,11 +174,12 @@ inline WsLayout ws_layout(int groups, int rpg, int V, int nch) {
   L.NR = (int64_t)groups * rpg;
   L.nsub = (V + kUnitB - 1) / kUnitB;
   // counters: row arrivals [NR], group arrivals [groups], CDF arrivals
-  // [groups], row cuts [NR], then the 8-byte chunk counters of both passes
-  size_t ncnt = 2 * (size_t)L.NR + 2 * (size_t)groups;
+  // [groups], row cuts [NR], group-ready flags [groups], then the 8-byte
+  // chunk counter
+  size_t ncnt = 2 * (size_t)L.NR + 3 * (size_t)groups;
   L.cnt_off = 0;
   L.ctr_off = (ncnt * sizeof(int) + 7) & ~(size_t)7;
-  L.cnt_bytes = align256(L.ctr_off + 2 * sizeof(unsigned long long));  // stream, CDF
+  L.cnt_bytes = align256(L.ctr_off + sizeof(unsigned long long));
   L.part_off = L.cnt_bytes;
   const size_t slots = nch > 1 ? (size_t)L.NR * nch : 1;
   L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));
@@ -180,9 +191,8 @@ inline WsLayout ws_layout(int groups, int rpg, int V, int nch) {
 }
 
 // ---- launchers (defined in ssd_stream.cu / ssd_cdf.cu / ssd_cache.cu) -----------
-cudaError_t launch_stream(const StreamParams& p, int dtype, int topk, int grid,
+cudaError_t launch_stream(const VerifyParams& p, int dtype, int topk, int grid,
                           cudaStream_t s);
-cudaError_t launch_cdf(const CdfParams& p, int dtype, int grid, cudaStream_t s);
 cudaError_t launch_cache_clear(void* table, int64_t capacity, cudaStream_t s);
 cudaError_t launch_cache_insert(void* table, int64_t capacity, const int32_t* row,
                                 const int32_t* k, const int32_t* t, const int32_t* branch, int n,
@@ -192,7 +202,6 @@ cudaError_t launch_cache_lookup(const void* table, int64_t capacity, const int32
                                 const int32_t* bonus, int B, int32_t* out_branch,
                                 int32_t* all_hit, cudaStream_t s);
 int stream_smem_bytes();
-int cdf_smem_bytes(int dtype);
 int num_sms();
 
 }  // namespace ssd

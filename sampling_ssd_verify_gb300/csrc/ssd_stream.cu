@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ssd_cdf_dev.cuh"
 #include "ssd_device.cuh"
 #include "ssd_internal.cuh"
 
@@ -441,6 +442,10 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
     }
     gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)k, 1u, p.round);
     p.gparams[g] = gp;
+    if (p.grp_ready) {
+      __threadfence();
+      flag_release(p.grp_ready + g);  // the group's draw may start
+    }
   }
 }
 
@@ -474,6 +479,10 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
   gp.scale_in = (float)scale_in;
   gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)p.jpos, 2u, p.round);
   p.gparams[g] = gp;
+  if (p.grp_ready) {
+    __threadfence();
+    flag_release(p.grp_ready + g);  // the row's draw may start
+  }
 }
 
 // Finalise row `row` from the merged (M, MC, S, top list) held by warp 0.
@@ -570,10 +579,15 @@ static_assert(kPieceQueue > kStagesA + 1, "piece queue shorter than the pipeline
 // A piece as the producer hands it to the consumer warps (chunk -1: the end).
 struct PieceDesc {
   long long chunk;
+  // a chunk of rows
   int64_t row, pu0, pu1;
   const char* rp;  // element 0 of the row
   int jr;          // row within its group
   int kch;         // chunk of the row
+  // a chunk of the draws: group g, units [u0, u1), the group's parameters
+  int64_t g;
+  int u0, u1;
+  GroupParams gp;
 };
 
 // Units [pu0, pu1) of row `row` that chunk c covers (chunks in the order
@@ -588,7 +602,12 @@ __device__ __forceinline__ void chunk_geom(const StreamParams& p, long long c, i
 
 template <int DT, int TOPK>
 __global__ void __launch_bounds__(kStreamThreads, 1)
-    stream_kernel(const __grid_constant__ StreamParams p) {
+    stream_kernel(const __grid_constant__ VerifyParams vp) {
+  const StreamParams& p = vp.s;
+  const CdfParams& cq = vp.q;  // the draws (cq.nchunks == 0: none)
+  const long long nS = p.nchunks;
+  const long long ntot = nS + cq.nchunks;
+  constexpr int kUps = fused_units_per_stage(Elem<DT>::kSize);  // units of a draw stage
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesA * kStageBytes);
@@ -637,8 +656,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       // copy does not wait behind every CTA's atomic on the counter
       unsigned long long next = blockIdx.x;
       for (int piece = 0;; ++piece) {
-        const long long c = next < (unsigned long long)p.nchunks ? (long long)next : -1ll;
+        long long c = next < (unsigned long long)ntot ? (long long)next : -1ll;
         PieceDesc& d = s_pq[piece % kPieceQueue];
+        if (c >= nS) {
+          // a chunk of the draws: wait until the epilogue of its group has
+          // published the group's parameters
+          int64_t g;
+          int u0, u1;
+          cdf_chunk_geom(cq, c - nS, g, u0, u1);
+          if (!SSD_CHK(g < cq.groups, p.dbg, 20, g, cq.groups) ||
+              !flag_wait(p.grp_ready + g, &s_err, p.status)) {
+            c = -1;
+          } else {
+            d.g = g;
+            d.u0 = u0;
+            d.u1 = u1;
+            d.gp = load_gp(cq.gp + g);
+          }
+        }
         d.chunk = c;
         if (c < 0) {
           // end marker: one stage without data
@@ -651,6 +686,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // the following chunk, fetched early (the counter hands out chunks
         // after the static first round)
         next = gridDim.x + atomicAdd(p.chunk_ctr, 1ull);
+        if (c >= nS) {
+          constexpr int ES = Elem<DT>::kSize;
+          const char* rt = d.gp.use_t ? row_ptr(cq.tgt, d.gp.row_t, cq.t_stride, ES) : nullptr;
+          const char* rd = d.gp.use_d ? row_ptr(cq.dft, d.gp.row_d, cq.d_stride, ES) : nullptr;
+          for (int u = d.u0, un = 0; u < d.u1; u = un) {
+            un = min(u + kUps, d.u1);
+            const int slot = n % kStagesA;
+            if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+            cdf_issue_stage<DT>(cq, rt, rd, u, un, ring + slot * kStageBytes, kStageBytes / 2,
+                                full + slot, &s_err);
+            ++n;
+          }
+          continue;
+        }
         int64_t row, pu0, pu1;
         int k;
         chunk_geom(p, c, row, k, pu0, pu1);
@@ -704,6 +753,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       const PieceRed<TOPK>& R = slots[slot];
       const long long chunk = R.chunk;
       if (chunk < 0) break;
+      if (chunk >= nS) {
+        // a chunk of the draws: its unit sums are stored; count it into its
+        // group, and draw if it completes the group
+        int64_t g;
+        int u0, u1;
+        cdf_chunk_geom(cq, chunk - nS, g, u0, u1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty + slot);
+        cdf_chunk_done<DT>(cq, g, u1 - u0);
+        continue;
+      }
       int64_t row, pu0, pu1;
       int kch;
       chunk_geom(p, chunk, row, kch, pu0, pu1);
@@ -806,6 +866,36 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (lane == 0) mbar_arrive(pfull + qs);
       }
       break;
+    }
+    if (chunk >= nS) {
+      // ---- a chunk of the draws: the weight sums of its units ----
+      const PieceDesc& dn = s_pq[piece % kPieceQueue];  // published by the stage's arrival
+      const int64_t g = dn.g;
+      const int u0 = dn.u0, u1 = dn.u1;
+      const GroupParams gp = dn.gp;
+      constexpr int ES = Elem<DT>::kSize;
+      const char* rt = gp.use_t ? row_ptr(cq.tgt, gp.row_t, cq.t_stride, ES) : nullptr;
+      const char* rd = gp.use_d ? row_ptr(cq.dft, gp.row_d, cq.d_stride, ES) : nullptr;
+      for (int u = u0, un = 0; u < u1; u = un) {
+        un = min(u + kUps, u1);
+        if (u != u0) mbar_wait(full + slot, phase, &s_err, p.status);
+        cdf_consume_stage<DT>(cq, g, gp, rt, rd, u, un, ring + slot * kStageBytes,
+                              kStageBytes / 2, warp);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + slot);
+        if (++slot == kStagesA) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      // hand the chunk to its epilogue warp
+      if (lane == 0 && piece >= kPieceSlots)
+        mbar_wait(pempty + ps, ((piece / kPieceSlots) - 1) & 1, &s_err, p.status);
+      __syncwarp();
+      if (warp == 0 && lane == 0) slots[ps].chunk = chunk;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull + ps);
+      continue;
     }
     const int64_t row = d.row, pu0 = d.pu0, pu1 = d.pu1;
     const int kch = d.kch;
@@ -965,17 +1055,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 }
 
 template <int DT, int TOPK>
-cudaError_t launch_t(const StreamParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_t(const VerifyParams& p, int grid, cudaStream_t s) {
   const int smem = stream_smem_bytes();
   auto kern = stream_kernel<DT, TOPK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kStreamThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  // CTAs wait for groups that other CTAs complete: all of them must be
+  // resident at once, which a cooperative launch guarantees
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = p.q.nchunks > 0 ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int DT>
-cudaError_t launch_dt(const StreamParams& p, int topk, int grid, cudaStream_t s) {
+cudaError_t launch_dt(const VerifyParams& p, int topk, int grid, cudaStream_t s) {
   switch (topk) {
     case 0: return launch_t<DT, 0>(p, grid, s);
     case 2: return launch_t<DT, 2>(p, grid, s);
@@ -993,7 +1094,7 @@ int stream_smem_bytes() {
          kPieceSlots * (int)sizeof(PieceRed<kMaxTopK>);
 }
 
-cudaError_t launch_stream(const StreamParams& p, int dtype, int topk, int grid, cudaStream_t s) {
+cudaError_t launch_stream(const VerifyParams& p, int dtype, int topk, int grid, cudaStream_t s) {
   return dtype == SSD_BF16 ? launch_dt<0>(p, topk, grid, s) : launch_dt<1>(p, topk, grid, s);
 }
 
