@@ -67,7 +67,7 @@ def _configure(L):
     L.orc_verify.argtypes = [_vp, _vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                              ctypes.c_double, _i32p, _u64p, ctypes.c_uint32, _i32p,
-                             ctypes.c_double, ctypes.c_int, _i32p, _i32p, _dp, _i32p, _dp,
+                             _dp, ctypes.c_int, _i32p, _i32p, _dp, _i32p, _dp,
                              _dp, _dp, ctypes.c_int, _i32p]
     L.orc_verify.restype = ctypes.c_int
     L.orc_topf_bonus.argtypes = [_vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
@@ -212,9 +212,20 @@ def _dtype_code(arr):
     raise TypeError(arr.dtype)
 
 
+def per_position_C(C, K):
+    """C as one Saguaro factor per draft position j = 0..K-1 (a scalar applies
+    to every position)."""
+    Cv = np.broadcast_to(np.asarray(C, dtype=np.float64), (K,)) if np.ndim(C) == 0 \
+        else np.asarray(C, dtype=np.float64)
+    if Cv.shape != (K,):
+        raise ValueError("C must be a scalar or have one entry per draft position")
+    return np.ascontiguousarray(Cv)
+
+
 def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1,
            row_ids=None):
-    """target [B,K+1,V], draft [B,Kq,V] (uint16 bf16 bits or float32)."""
+    """target [B,K+1,V], draft [B,Kq,V] (uint16 bf16 bits or float32); C a
+    scalar or one factor per draft position."""
     target = np.ascontiguousarray(target)
     draft = np.ascontiguousarray(draft)
     B, K1, V = target.shape
@@ -232,9 +243,10 @@ def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1,
     gq = np.zeros((B, Kq, Fmax))
     ma = np.zeros(B)
     mc = np.zeros(B)
+    Cv = per_position_C(C, K)
     rc = lib().orc_verify(target.ctypes.data, draft.ctypes.data, _dtype_code(target), V, V, B, K,
                           Kq, V, float(T), _p(tokens, _i32p), _p(seeds, _u64p), int(round_),
-                          _p(F, _i32p), float(C), Fmax, _p(acc, _i32p), _p(bon, _i32p),
+                          _p(F, _i32p), _p(Cv, _dp), Fmax, _p(acc, _i32p), _p(bon, _i32p),
                           _p(Z, _dp), _p(g, _i32p), _p(gq, _dp), _p(ma, _dp), _p(mc, _dp),
                           int(nthreads), _p(None if row_ids is None else _i32(row_ids), _i32p))
     if rc:
@@ -306,13 +318,15 @@ def draft_tokens(draft, F, C, T, seeds, round_=0, K=None, nthreads=1):
 
     draft [B, Kq, V]; row (b, j) uses counter (b, j, 2, round) -- the same
     definition as the library's continuation sampler called once per position.
+    C: a scalar or one factor per draft position.
     """
     draft = np.ascontiguousarray(draft)
     B, Kq, V = draft.shape
     K = Kq - 1 if K is None else K
+    Cv = per_position_C(C, K)
     out = np.zeros((B, K), dtype=np.int32)
     for j in range(K):
-        r = saguaro_sample(np.ascontiguousarray(draft[:, j, :]), T, C, int(F[j]), seeds, j,
+        r = saguaro_sample(np.ascontiguousarray(draft[:, j, :]), T, Cv[j], int(F[j]), seeds, j,
                            round_, nthreads=nthreads)
         out[:, j] = r["token"]
     return out

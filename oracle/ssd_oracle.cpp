@@ -283,7 +283,10 @@ int orc_inverse_cdf(const double* w, int V, double Z, double u, double* margin) 
 // (b*Kq+j)*d_stride.  F: [Kq] fan-out (F[K] used only when Kq == K+1).
 // For sequence b:
 //   p_i = softmax(z_p[i]/T), q_j = softmax(z_q[j]/T)
-//   S_j = top-F_j of z_q[j];  q'_j = Saguaro(q_j, S_j, C)
+//   S_j = top-F_j of z_q[j];  q'_j = Saguaro(q_j, S_j, C_j)
+//   (C: one Saguaro factor per draft position j = 0..K-1 -- a single C for
+//   every position is the pages' setting, a factor per position the
+//   extension [SSD-note] §"关于逐位置 C 的思考" proposes)
 //   i = 0..K-1: u = U(seed_b; b, i, 0, round); accept iff u < p_i(x_i)/q'_i(x_i),
 //               else k = i and stop ([SD-7.3] §7.3.2 step 4: later drafts dropped);
 //               all accepted -> k = K
@@ -299,7 +302,7 @@ int orc_inverse_cdf(const double* w, int V, double Z, double u, double* margin) 
 int orc_verify(const void* target, const void* draft, int dtype, int64_t t_stride,
                int64_t d_stride, int B, int K, int Kq, int V, double T,
                const int32_t* tokens, const uint64_t* seeds, uint32_t round,
-               const int32_t* F, double C, int Fmax, int32_t* accept_len, int32_t* bonus,
+               const int32_t* F, const double* C, int Fmax, int32_t* accept_len, int32_t* bonus,
                double* resid_mass, int32_t* guesses, double* guess_q, double* margin_accept,
                double* margin_cdf, int nthreads, const int32_t* row_ids) {
   for (int i = 0; i < B * K; ++i)
@@ -322,7 +325,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
       auto zp = load_row(target, dtype, ((int64_t)b * (K + 1) + i) * t_stride, V);
       auto p = softmax(zp, T);
       std::vector<int> S(top1[i].begin(), top1[i].begin() + std::min<int>(F[i], top1[i].size()));
-      auto qp = saguaro(q[i], S, C);
+      auto qp = saguaro(q[i], S, C[i]);
       double r = p[x[i]] / qp[x[i]];
       double u = uniform24(seeds[b], rid, (uint32_t)i, 0u, round);
       mA = std::min(mA, std::fabs(u - r));

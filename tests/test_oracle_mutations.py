@@ -24,6 +24,8 @@ MUTATIONS = {
     "philox key bump dropped": ("k[1] += PhiloxConst<W>::W1;", ""),
     "philox words swapped": ("c[1] = lo1;", "c[1] = lo0;"),
     "fanout exponent": ("(double)k / (1.0 + r)", "(double)k / r"),
+    "per-position C collapsed to the first": ("auto qp = saguaro(q[i], S, C[i]);",
+                                              "auto qp = saguaro(q[i], S, C[0]);"),
 }
 
 PINS = [
@@ -36,6 +38,7 @@ PINS = [
     P.test_inverse_cdf_matches_library_search,
     lambda orc: P.test_losslessness_exact_enumeration(orc, 5, 3, 0.5, 1.0),
     P.test_fanout_is_the_lagrange_optimum,
+    lambda orc: P.test_accept_length_law_per_position_C(orc, (0.3, 0.5, 0.8, 1.0)),
 ]
 
 

@@ -276,6 +276,42 @@ def test_accept_length_law_monte_carlo(orc):
     assert abs(z) < 4
 
 
+@pytest.mark.parametrize("Cv", [(0.3, 0.5, 0.8, 1.0), (1.0, 0.2, 1.0, 0.6)])
+def test_accept_length_law_per_position_C(orc, Cv):
+    """One Saguaro factor per draft position ([SSD-note] §"关于逐位置 C 的思考"
+    proposes it): drafts drawn from q'_j built with C_j and verified against
+    the same q'_j keep the accept-length law P(k >= j) = prod_{i<j} alpha_i,
+    alpha_i = sum min(p_i, q'_i(C_i)), and every emitted token still follows
+    p_j.  Config-1 shapes, 10^5 seeded rows."""
+    w = WORKLOADS["c1"]
+    bt = make_batch(w)
+    zp = bt["target"][0].astype(np.float64)
+    zq = bt["draft"][0].astype(np.float64)
+    K, F, T = w.K, bt["fanout"], w.T
+    p = [orc.softmax(zp[i], T) for i in range(K + 1)]
+    qp = [orc.saguaro_dist(zq[j], T, int(F[j]), Cv[j]) for j in range(K)]
+    pk = _accept_law(p, qp, K)
+    n = 50_000
+    tgt, dft = _replicated_batch(bt["target"][0], bt["draft"][0], n)
+    seeds = np.arange(n, dtype=np.uint64) * 6007 + 5
+    ks, ts, xs = [], [], []
+    for rnd in range(2):
+        tok = orc.draft_tokens(dft, F, Cv, T, seeds, round_=rnd, K=K)
+        r = orc.verify(tgt, dft, tok, seeds, rnd, F, Cv, T, nthreads=8)
+        ks.append(r["accept_len"]); ts.append(r["bonus"]); xs.append(tok)
+    ks, ts, xs = np.concatenate(ks), np.concatenate(ts), np.concatenate(xs)
+    hist = np.bincount(ks, minlength=K + 1)
+    assert stats.chisquare(hist, pk * len(ks)).pvalue > 1e-4
+    V = zp.shape[1]
+    for j in range(K + 1):
+        reached = ks >= j
+        emit = np.where(ks[reached] > j, xs[reached][:, min(j, K - 1)], ts[reached])
+        obs = np.bincount(emit, minlength=V)
+        m = p[j] * reached.sum() > 5
+        stat = stats.chisquare(obs[m], p[j][m] / p[j][m].sum() * obs[m].sum())
+        assert stat.pvalue > 1e-4, (j, stat)
+
+
 def test_bonus_law_monte_carlo(orc):
     """Given rejection at i the bonus follows normalize((p_i - q'_i)^+); given
     all accepted it follows p_K ([SD-7.3] §7.3.3).  Chi-square over 10^6
