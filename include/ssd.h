@@ -137,6 +137,28 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
                       void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ssd_verify_ck -- ssd_verify with one Saguaro factor per draft position.
+ * [SSD-note] §"关于逐位置 C 的思考": the pages use one global C and propose a
+ * factor per position (positions whose fan-out covers more can bias less).
+ *
+ * As ssd_verify, with q'_j built from C_pos[j] instead of C:
+ *   q'_j(y) = q_j(y) * (C_j if y in S_j else 1) / (1 - (1-C_j) * q_j(S_j)).
+ * The drafts x_j must have been drawn from the same q'_j (for example by
+ * ssd_saguaro_sample at position j with C = C_pos[j]).
+ *
+ * C_pos  HOST [K] float, each in (0, 1]; read before the call returns.
+ * Every C_pos[j] equal to C gives the results of ssd_verify with C, bit for
+ * bit.  Other arguments, errors and outputs: ssd_verify.
+ * ------------------------------------------------------------------------- */
+ssd_status ssd_verify_ck(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                         int Kq, int V, float T, const int32_t* draft_tokens,
+                         const uint64_t* seeds, uint32_t round, const int32_t* fanout,
+                         const float* C_pos, int32_t* accept_len, int32_t* bonus,
+                         float* resid_mass, int32_t* guesses, float* guess_q, int Fmax,
+                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
  * ssd_verify_noalloc -- ssd_verify without a caller workspace.  The pages have
  * no counterpart: this is a deployment convenience.
  *

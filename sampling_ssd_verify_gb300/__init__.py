@@ -61,6 +61,8 @@ _SIGS = {
     "ssd_verify_workspace_size": ([_i, _i, _i, _i], _sz),
     "ssd_verify": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32, _vp,
                     ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
+    "ssd_verify_ck": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32, _vp,
+                       _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "ssd_topf_workspace_size": ([_i, _i, _i], _sz),
     "ssd_topf_bonus": ([_LP, _i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, _vp, _vp, _vp, _sz,
                         _vp, _vp], _i),
@@ -175,6 +177,8 @@ def verify(target, draft, draft_tokens, seeds, round_, fanout=None, C=1.0, T=1.0
 
     target [B, K+1, V], draft [B, Kq, V] (bf16 or fp32, same dtype),
     draft_tokens int32 [B, K], seeds 64-bit [B], fanout: sequence of Kq ints.
+    C: the Saguaro factor, or a sequence of K factors, one per draft position
+    (ssd_verify_ck).
     Returns a dict of device tensors: accept_len, bonus, resid_mass, guesses,
     guess_q (the optional ones only when requested).
     """
@@ -204,14 +208,21 @@ def verify(target, draft, draft_tokens, seeds, round_, fanout=None, C=1.0, T=1.0
         raise SSDError("invalid verify shape")
     ws = workspace if workspace is not None else _workspace(wsb, dev)
     tl, dl = _logits(target), _logits(draft)
-    st = L.ssd_verify(ctypes.byref(tl), ctypes.byref(dl), B, K, Kq, V, float(T),
-                      _dev_ptr(_i32(draft_tokens)), _dev_ptr(_u64_seeds(seeds, dev)),
-                      int(round_) & 0xFFFFFFFF, F.ctypes.data_as(ctypes.c_void_p), float(C),
-                      _dev_ptr(o["accept_len"]), _dev_ptr(o["bonus"]),
-                      _dev_ptr(o.get("resid_mass")), _dev_ptr(o.get("guesses")),
-                      _dev_ptr(o.get("guess_q")), Fmax, _dev_ptr(ws), ws.numel(),
-                      _dev_ptr(dev_status), _stream(stream))
-    _check(st, "ssd_verify")
+    if np.ndim(C) == 0:
+        fn, c_arg, name = L.ssd_verify, float(C), "ssd_verify"
+    else:
+        Cv = np.ascontiguousarray(C, dtype=np.float32)
+        if Cv.shape != (K,):
+            raise SSDError("C must be a scalar or have one entry per draft position")
+        fn, c_arg, name = L.ssd_verify_ck, Cv.ctypes.data_as(ctypes.c_void_p), "ssd_verify_ck"
+    st = fn(ctypes.byref(tl), ctypes.byref(dl), B, K, Kq, V, float(T),
+            _dev_ptr(_i32(draft_tokens)), _dev_ptr(_u64_seeds(seeds, dev)),
+            int(round_) & 0xFFFFFFFF, F.ctypes.data_as(ctypes.c_void_p), c_arg,
+            _dev_ptr(o["accept_len"]), _dev_ptr(o["bonus"]),
+            _dev_ptr(o.get("resid_mass")), _dev_ptr(o.get("guesses")),
+            _dev_ptr(o.get("guess_q")), Fmax, _dev_ptr(ws), ws.numel(),
+            _dev_ptr(dev_status), _stream(stream))
+    _check(st, name)
     return o
 
 

@@ -270,17 +270,24 @@ size_t ssd_saguaro_workspace_size(int R, int V) {
   return ws_layout(R, 1, V, stream_chunks_per_row((int64_t)R, units_per_row(V))).total;
 }
 
-ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,
-                      int V, float T, const int32_t* draft_tokens, const uint64_t* seeds,
-                      uint32_t round, const int32_t* fanout, float C, int32_t* accept_len,
-                      int32_t* bonus, float* resid_mass, int32_t* guesses, float* guess_q,
-                      int Fmax, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                      void* stream) {
+}  // extern "C"
+
+namespace {
+
+// ssd_verify with a Saguaro factor per draft position (Cv[0..K-1], host).
+ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,
+                       int V, float T, const int32_t* draft_tokens, const uint64_t* seeds,
+                       uint32_t round, const int32_t* fanout, const float* Cv,
+                       int32_t* accept_len, int32_t* bonus, float* resid_mass, int32_t* guesses,
+                       float* guess_q, int Fmax, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_status, void* stream) {
   if (B < 1 || K < 1 || K > SSD_MAX_K || (Kq != K && Kq != K + 1) || V < 2 || V > SSD_MAX_V)
     return SSD_ERR_INVALID_ARG;
   if (!logits_ok(target, V) || !logits_ok(draft, V) || target->dtype != draft->dtype)
     return SSD_ERR_INVALID_ARG;
-  if (!finite_pos(T) || !std::isfinite(C) || !(C > 0.f) || C > 1.f) return SSD_ERR_INVALID_ARG;
+  if (!finite_pos(T) || Cv == nullptr) return SSD_ERR_INVALID_ARG;
+  for (int j = 0; j < K; ++j)
+    if (!std::isfinite(Cv[j]) || !(Cv[j] > 0.f) || Cv[j] > 1.f) return SSD_ERR_INVALID_ARG;
   if (!draft_tokens || !seeds || !accept_len || !bonus) return SSD_ERR_INVALID_ARG;
   if (guess_q && !guesses) return SSD_ERR_INVALID_ARG;
   int F[SSD_MAX_K + 1] = {0};
@@ -294,9 +301,10 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
     }
   }
   if (guesses && (Fmax < 1 || Fmax < maxF)) return SSD_ERR_INVALID_ARG;
-  int maxF_verify = 0;
-  for (int j = 0; j < K; ++j) maxF_verify = std::max(maxF_verify, F[j]);
-  const bool need_top = (guesses && maxF > 0) || (C < 1.f && maxF_verify > 0);
+  // top lists are needed for the guesses and for every position that biases
+  bool biased = false;
+  for (int j = 0; j < K; ++j) biased |= Cv[j] < 1.f && F[j] > 0;
+  const bool need_top = (guesses && maxF > 0) || biased;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Common cm;
   WsLayout L;
@@ -304,8 +312,10 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
                         cm, L);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
-  for (int j = 0; j <= SSD_MAX_K; ++j) p.F[j] = F[j];
-  p.C = C;
+  for (int j = 0; j <= SSD_MAX_K; ++j) {
+    p.F[j] = F[j];
+    p.C[j] = j < K ? Cv[j] : 1.f;
+  }
   p.need_top = need_top ? 1 : 0;
   p.tokens = draft_tokens;
   p.tokK = K;
@@ -323,6 +333,37 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
   q.out_mass = resid_mass;
   q.status = dev_status;
   return run_pass(cm, target->dtype, need_top ? topk_for(maxF) : 0, true, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,
+                      int V, float T, const int32_t* draft_tokens, const uint64_t* seeds,
+                      uint32_t round, const int32_t* fanout, float C, int32_t* accept_len,
+                      int32_t* bonus, float* resid_mass, int32_t* guesses, float* guess_q,
+                      int Fmax, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      void* stream) {
+  if (K < 1 || K > SSD_MAX_K) return SSD_ERR_INVALID_ARG;
+  float Cv[SSD_MAX_K];
+  for (int j = 0; j < K; ++j) Cv[j] = C;
+  return verify_impl(target, draft, B, K, Kq, V, T, draft_tokens, seeds, round, fanout, Cv,
+                     accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+                     workspace_bytes, dev_status, stream);
+}
+
+ssd_status ssd_verify_ck(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                         int Kq, int V, float T, const int32_t* draft_tokens,
+                         const uint64_t* seeds, uint32_t round, const int32_t* fanout,
+                         const float* C_pos, int32_t* accept_len, int32_t* bonus,
+                         float* resid_mass, int32_t* guesses, float* guess_q, int Fmax,
+                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                         void* stream) {
+  if (K < 1 || K > SSD_MAX_K || C_pos == nullptr) return SSD_ERR_INVALID_ARG;
+  return verify_impl(target, draft, B, K, Kq, V, T, draft_tokens, seeds, round, fanout, C_pos,
+                     accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+                     workspace_bytes, dev_status, stream);
 }
 
 ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T,
@@ -347,8 +388,10 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
   ssd_status st = setup(nullptr, draft, B, 0, Kq, 0, Kq, V, T, workspace, workspace_bytes, s, cm, L);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
-  for (int j = 0; j <= SSD_MAX_K; ++j) p.F[j] = F[j];
-  p.C = 1.f;
+  for (int j = 0; j <= SSD_MAX_K; ++j) {
+    p.F[j] = F[j];
+    p.C[j] = 1.f;
+  }
   p.need_top = maxF > 0;
   p.tokens = draft_tokens;
   p.tokK = draft_tokens ? K : 0;
@@ -375,7 +418,7 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
   p.F[0] = F;
-  p.C = C;
+  for (int j = 0; j <= SSD_MAX_K; ++j) p.C[j] = j == 0 ? C : 1.f;
   const bool need_top = F > 0;
   p.need_top = need_top;
   p.seeds = seeds;

@@ -86,7 +86,7 @@ struct StreamParams {
   unsigned long long* chunk_ctr;
   uint32_t* row_cut;        // per row: ordered-float lower bound on its top-list cut (0: none)
   float c;                  // log2(e) / T
-  float C;
+  float C[SSD_MAX_K + 1];   // Saguaro factor per draft position (a continuation draw: C[0])
   int F[SSD_MAX_K + 1];
   int need_top;             // draft rows keep a top list
   const int32_t* tokens;    // [groups, tokK] or null

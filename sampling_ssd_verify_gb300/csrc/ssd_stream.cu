@@ -384,7 +384,8 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
     const double mcq = (double)__ldcg(&rd->mc);
     double qp = exp2((double)__ldcg(&rd->zx) * c - mcq) / sq;
     const int F = p.F[lane];
-    if (p.C < 1.f && F > 0) {
+    const float Cl = p.C[lane];
+    if (Cl < 1.f && F > 0) {
       double QS = 0.0;
       bool inS = false;
       for (int f = 0; f < F; ++f) {
@@ -392,7 +393,7 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
         inS |= __ldcg(&rd->ti[f]) == x;
       }
       QS /= sq;
-      qp = qp * (inS ? (double)p.C : 1.0) / (1.0 - (1.0 - (double)p.C) * QS);
+      qp = qp * (inS ? (double)Cl : 1.0) / (1.0 - (1.0 - (double)Cl) * QS);
     }
     const double r = pt / qp;
     const double u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)lane, 0u, p.round);
@@ -421,14 +422,15 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
       const double sq = __ldcg(&rd->s);
       double scale_out = 1.0 / sq, scale_in = 1.0 / sq;
       const int F = p.F[k];
-      if (p.C < 1.f && F > 0) {
+      const float Ck = p.C[k];
+      if (Ck < 1.f && F > 0) {
         double QS = 0.0;
         for (int f = 0; f < F; ++f)
           QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), p.c, -gp.mc_d));
         QS /= sq;
-        const double gn = 1.0 / (1.0 - (1.0 - (double)p.C) * QS);
+        const double gn = 1.0 / (1.0 - (1.0 - (double)Ck) * QS);
         scale_out = gn / sq;
-        scale_in = gn * (double)p.C / sq;
+        scale_in = gn * (double)Ck / sq;
         gp.theta = __ldcg(&rd->tv[F - 1]);
         gp.itheta = __ldcg(&rd->ti[F - 1]);
       }
@@ -465,13 +467,14 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
   gp.itheta = -1;
   double scale_out = 1.0 / rr.s, scale_in = 1.0 / rr.s;
   const int F = p.F[0];
-  if (p.C < 1.f && F > 0) {
+  const float C = p.C[0];
+  if (C < 1.f && F > 0) {
     double QS = 0.0;
     for (int f = 0; f < F; ++f) QS += (double)exp2f(fmaf(rr.tv[f], p.c, -rr.mc));
     QS /= rr.s;
-    const double gn = 1.0 / (1.0 - (1.0 - (double)p.C) * QS);
+    const double gn = 1.0 / (1.0 - (1.0 - (double)C) * QS);
     scale_out = gn / rr.s;
-    scale_in = gn * (double)p.C / rr.s;
+    scale_in = gn * (double)C / rr.s;
     gp.theta = rr.tv[F - 1];
     gp.itheta = rr.ti[F - 1];
   }

@@ -137,6 +137,26 @@ def test_verify_rejects_bad_arguments_on_the_host(L):
     assert _verify(L, ws=0x1000, wsb=16) == 5                # too small
 
 
+def _verify_ck(L, Cv, K=4, Kq=5):
+    C = None if Cv is None else np.asarray(Cv, dtype=np.float32)
+    t, d = _fake(), _fake()
+    return L.ssd_verify_ck(ctypes.byref(t), ctypes.byref(d), 1, K, Kq, 32, 1.0, 0x20000, 0x30000,
+                           0, None, None if C is None else C.ctypes.data_as(ctypes.c_void_p),
+                           0x40000, 0x50000, None, None, None, 1, None, 0, None, None)
+
+
+def test_verify_ck_rejects_bad_factors_on_the_host(L):
+    """Every per-position factor must lie in (0, 1]; a missing vector is an
+    argument error.  Valid factors get as far as the (missing) workspace."""
+    inv = 1
+    assert _verify_ck(L, None) == inv
+    assert _verify_ck(L, [0.5, 0.5, 0.0, 0.5]) == inv
+    assert _verify_ck(L, [0.5, 1.5, 0.5, 0.5]) == inv
+    assert _verify_ck(L, [0.5, 0.5, 0.5, float("nan")]) == inv
+    assert _verify_ck(L, [0.5, 0.5, 0.5, 0.5], K=0, Kq=0) == inv
+    assert _verify_ck(L, [0.3, 0.5, 1.0, 0.7]) == 5
+
+
 def test_other_entry_points_reject_bad_arguments(L):
     d = _fake()
     F = np.array([1, 1], dtype=np.int32)

@@ -182,6 +182,33 @@ def test_plain_sd_is_bit_identical_with_c1_or_empty_sets(orc):
         np.testing.assert_array_equal(a[k], b[k])
 
 
+@pytest.mark.parametrize("name,B,V,dtype,Cv", [
+    ("c1", 4000, 32, "f32", (0.3, 0.5, 0.8, 1.0)),
+    ("c5", 24, 151936, "f32", (0.2, 0.3, 0.5, 0.5, 0.7, 0.9, 1.0, 1.0)),
+    ("c3", 12, 128256, "bf16", (0.3, 1.0, 0.5, 1.0, 0.7, 0.2, 1.0, 0.4)),
+], ids=["c1-shape", "c5-shape", "c3-shape"])
+def test_per_position_C(orc, name, B, V, dtype, Cv):
+    """ssd_verify_ck: one Saguaro factor per draft position ([SSD-note]
+    §"关于逐位置 C 的思考"), drafts drawn with the same factors, against the
+    oracle row by row."""
+    run_verify(orc, WORKLOADS[name], B=B, V=V, dtype=dtype, C=np.array(Cv), rounds=(0, 1))
+
+
+def test_per_position_C_equal_entries_match_scalar(orc):
+    """Every per-position factor equal to C gives ssd_verify's outputs with C,
+    bit for bit (guesses, their probabilities and residual masses included)."""
+    torch, dev = torch_dev()
+    w = WORKLOADS["c5"]
+    bt = make_batch(w, B=16, V=30000)
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=w.K)
+    tg, dg = upload(bt["target"], "f32"), upload(bt["draft"], "f32")
+    a = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 2, F, w.C, w.T))
+    b = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 2, F, np.full(w.K, w.C), w.T))
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
+
+
 def test_bad_token_sets_status(orc):
     torch, dev = torch_dev()
     w = WORKLOADS["c1"]
