@@ -68,7 +68,7 @@ def _configure(L):
                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                              ctypes.c_double, _i32p, _u64p, ctypes.c_uint32, _i32p,
                              _dp, ctypes.c_int, _i32p, _i32p, _dp, _i32p, _dp,
-                             _dp, _dp, ctypes.c_int, _i32p]
+                             _dp, _dp, ctypes.c_int, _i32p, _dp]
     L.orc_verify.restype = ctypes.c_int
     L.orc_topf_bonus.argtypes = [_vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_double, _i32p,
@@ -225,7 +225,8 @@ def per_position_C(C, K):
 def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1,
            row_ids=None):
     """target [B,K+1,V], draft [B,Kq,V] (uint16 bf16 bits or float32); C a
-    scalar or one factor per draft position."""
+    scalar or one factor per draft position; T a scalar or one temperature
+    per sequence (0: the greedy limit)."""
     target = np.ascontiguousarray(target)
     draft = np.ascontiguousarray(draft)
     B, K1, V = target.shape
@@ -244,11 +245,19 @@ def verify(target, draft, tokens, seeds, round_, F, C, T, Fmax=None, nthreads=1,
     ma = np.zeros(B)
     mc = np.zeros(B)
     Cv = per_position_C(C, K)
+    if np.ndim(T) == 0:
+        T0, Tr = float(T), None
+    else:
+        Tr = np.ascontiguousarray(T, dtype=np.float64)
+        if Tr.shape != (B,):
+            raise ValueError("T must be a scalar or have one entry per sequence")
+        T0 = 1.0
     rc = lib().orc_verify(target.ctypes.data, draft.ctypes.data, _dtype_code(target), V, V, B, K,
-                          Kq, V, float(T), _p(tokens, _i32p), _p(seeds, _u64p), int(round_),
+                          Kq, V, T0, _p(tokens, _i32p), _p(seeds, _u64p), int(round_),
                           _p(F, _i32p), _p(Cv, _dp), Fmax, _p(acc, _i32p), _p(bon, _i32p),
                           _p(Z, _dp), _p(g, _i32p), _p(gq, _dp), _p(ma, _dp), _p(mc, _dp),
-                          int(nthreads), _p(None if row_ids is None else _i32(row_ids), _i32p))
+                          int(nthreads), _p(None if row_ids is None else _i32(row_ids), _i32p),
+                          _p(Tr, _dp))
     if rc:
         raise ValueError("draft token outside [0, V)")
     return dict(accept_len=acc, bonus=bon, resid_mass=Z, guesses=g, guess_q=gq,

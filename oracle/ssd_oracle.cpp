@@ -298,24 +298,66 @@ int orc_inverse_cdf(const double* w, int V, double Z, double u, double* margin) 
 // ([SSD-note] §"解法：操纵草稿分布": lowering q on cached tokens raises (p-q)^+).
 // row_ids (or NULL = 0..B-1) give each row's Philox counter word 0, so a
 // sample of rows of a larger batch can be checked one by one.
+//
+// T_rows (or NULL: T for every row) gives each sequence its own temperature.
+// T = 0 is the greedy limit T -> 0 (a common serving setting; the pages do
+// not treat it): p_i and q_j become one-hot at the argmax of their logits
+// (ties to the lower index, the top-n order), so
+//   x_i is accepted iff x_i = argmax z_p[i] (p_i(x_i) / q'_i(x_i) is 1 for a
+//   greedy draft on the target's argmax and 0 otherwise; Saguaro's factor
+//   leaves a one-hot q unchanged),
+//   the bonus is argmax z_p[k] (the residual of a one-hot p_k against a
+//   one-hot q'_k at another token is p_k itself; all accepted: p_K),
+//   resid_mass = 1, both margins = +inf (no random decision), and guess_q is
+//   the limit of q_j: 1 for the draft argmax, 0 for every other guess.
 // Returns 0, or 1 if a draft token lies outside [0, V).
 int orc_verify(const void* target, const void* draft, int dtype, int64_t t_stride,
                int64_t d_stride, int B, int K, int Kq, int V, double T,
                const int32_t* tokens, const uint64_t* seeds, uint32_t round,
                const int32_t* F, const double* C, int Fmax, int32_t* accept_len, int32_t* bonus,
                double* resid_mass, int32_t* guesses, double* guess_q, double* margin_accept,
-               double* margin_cdf, int nthreads, const int32_t* row_ids) {
+               double* margin_cdf, int nthreads, const int32_t* row_ids, const double* T_rows) {
   for (int i = 0; i < B * K; ++i)
     if (tokens[i] < 0 || tokens[i] >= V) return 1;
   parallel_rows(B, nthreads, [&](int b) {
+    const double Tb = T_rows ? T_rows[b] : T;
     std::vector<std::vector<double>> zq(Kq), q(Kq);
     std::vector<std::vector<int>> top1(Kq);
     for (int j = 0; j < Kq; ++j) {
       zq[j] = load_row(draft, dtype, ((int64_t)b * Kq + j) * d_stride, V);
-      q[j] = softmax(zq[j], T);
+      if (Tb > 0.0) q[j] = softmax(zq[j], Tb);
       top1[j] = top_n(zq[j], F[j] + 1);
     }
     const int32_t* x = tokens + (int64_t)b * K;
+    if (Tb == 0.0) {
+      int k = K;
+      for (int i = 0; i < K; ++i) {
+        auto zp = load_row(target, dtype, ((int64_t)b * (K + 1) + i) * t_stride, V);
+        if (x[i] != top_n(zp, 1)[0]) {
+          k = i;
+          break;
+        }
+      }
+      auto zk = load_row(target, dtype, ((int64_t)b * (K + 1) + k) * t_stride, V);
+      accept_len[b] = k;
+      bonus[b] = top_n(zk, 1)[0];
+      if (resid_mass) resid_mass[b] = 1.0;
+      if (margin_accept) margin_accept[b] = INFINITY;
+      if (margin_cdf) margin_cdf[b] = INFINITY;
+      if (guesses) {
+        for (int j = 0; j < Kq; ++j) {
+          int excl = j < K ? x[j] : -1;
+          auto g = guesses_from(top1[j], F[j], excl);
+          const int amax = top_n(zq[j], 1)[0];
+          for (int f = 0; f < Fmax; ++f) {
+            int64_t o = ((int64_t)b * Kq + j) * Fmax + f;
+            guesses[o] = f < (int)g.size() ? g[f] : -1;
+            if (guess_q) guess_q[o] = (f < (int)g.size() && g[f] == amax) ? 1.0 : 0.0;
+          }
+        }
+      }
+      return;
+    }
     const uint32_t rid = row_ids ? (uint32_t)row_ids[b] : (uint32_t)b;  // Philox counter word 0
     int k = K;
     double mA = INFINITY;
@@ -323,7 +365,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
     std::vector<double> qp_k;
     for (int i = 0; i < K; ++i) {
       auto zp = load_row(target, dtype, ((int64_t)b * (K + 1) + i) * t_stride, V);
-      auto p = softmax(zp, T);
+      auto p = softmax(zp, Tb);
       std::vector<int> S(top1[i].begin(), top1[i].begin() + std::min<int>(F[i], top1[i].size()));
       auto qp = saguaro(q[i], S, C[i]);
       double r = p[x[i]] / qp[x[i]];
@@ -342,7 +384,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
       Z = residual(p_k, qp_k, w);
     } else {
       auto zp = load_row(target, dtype, ((int64_t)b * (K + 1) + K) * t_stride, V);
-      w = softmax(zp, T);
+      w = softmax(zp, Tb);
       Z = 0.0;
       for (double v : w) Z += v;
     }
@@ -354,7 +396,7 @@ int orc_verify(const void* target, const void* draft, int dtype, int64_t t_strid
     } else {
       // degenerate residual (cannot happen in exact arithmetic): draw from p_k
       auto zp = load_row(target, dtype, ((int64_t)b * (K + 1) + k) * t_stride, V);
-      auto p = softmax(zp, T);
+      auto p = softmax(zp, Tb);
       double Zp = 0.0;
       for (double v : p) Zp += v;
       t = inverse_cdf(p, Zp, u2, &mC);

@@ -26,6 +26,10 @@ MUTATIONS = {
     "fanout exponent": ("(double)k / (1.0 + r)", "(double)k / r"),
     "per-position C collapsed to the first": ("auto qp = saguaro(q[i], S, C[i]);",
                                               "auto qp = saguaro(q[i], S, C[0]);"),
+    "per-sequence temperature ignored": ("const double Tb = T_rows ? T_rows[b] : T;",
+                                         "const double Tb = T;"),
+    "greedy bonus from the runner-up": ("bonus[b] = top_n(zk, 1)[0];",
+                                        "bonus[b] = top_n(zk, 2)[1];"),
 }
 
 PINS = [
@@ -39,6 +43,8 @@ PINS = [
     lambda orc: P.test_losslessness_exact_enumeration(orc, 5, 3, 0.5, 1.0),
     P.test_fanout_is_the_lagrange_optimum,
     lambda orc: P.test_accept_length_law_per_position_C(orc, (0.3, 0.5, 0.8, 1.0)),
+    P.test_greedy_is_the_low_temperature_limit,
+    P.test_per_sequence_temperature_equals_separate_calls,
 ]
 
 

@@ -312,6 +312,82 @@ def test_accept_length_law_per_position_C(orc, Cv):
         assert stat.pvalue > 1e-4, (j, stat)
 
 
+def _greedy_case(V=40, K=4, B=64, seed=31):
+    """Logits whose two largest entries are at least 0.5 apart, with the
+    draft's argmax equal to the target's at about half the positions."""
+    rng = np.random.default_rng(seed)
+    zp = rng.normal(0, 1, (B, K + 1, V))
+    zq = zp + rng.normal(0, 0.5, (B, K + 1, V))
+    for z in (zp, zq):
+        top = z.argmax(-1)
+        np.put_along_axis(z, top[..., None], z.max(-1, keepdims=True) + 0.5, -1)
+    agree = rng.random((B, K + 1)) < 0.6
+    ia = zp.argmax(-1)
+    for b in range(B):
+        for j in range(K + 1):
+            if agree[b, j]:   # move the draft's peak onto the target's argmax
+                zq[b, j, ia[b, j]] = zq[b, j].max() + 0.5
+    return zp, zq
+
+
+def test_greedy_is_the_low_temperature_limit(orc):
+    """T = 0 is the limit T -> 0: with greedy drafts (x_j = argmax z_q[j])
+    the stochastic verify at T = 0.005 (top-2 gaps >= 0.5, so p and q are
+    one-hot to e^-100) gives the same accept lengths and bonus tokens as the
+    greedy verify, for every seed and C."""
+    zp, zq = _greedy_case()
+    B, K1, V = zp.shape
+    K = K1 - 1
+    tok = zq[:, :K].argmax(-1).astype(np.int32)
+    seeds = np.arange(B, dtype=np.uint64) * 977 + 1
+    F = np.array([3, 2, 2, 1, 1], dtype=np.int32)
+    for C in (1.0, 0.4):
+        g = orc.verify(zp.astype(np.float32), zq.astype(np.float32), tok, seeds, 0, F, C, 0.0)
+        for rnd in range(3):
+            s_ = orc.verify(zp.astype(np.float32), zq.astype(np.float32), tok, seeds, rnd, F, C,
+                            0.005)
+            np.testing.assert_array_equal(g["accept_len"], s_["accept_len"])
+            np.testing.assert_array_equal(g["bonus"], s_["bonus"])
+    assert 0 < g["accept_len"].mean() < K
+    np.testing.assert_array_equal(g["resid_mass"], 1.0)
+
+
+def test_greedy_ties_go_to_the_lower_index(orc):
+    """The greedy argmax breaks ties as numpy.argmax does (first occurrence),
+    with heavily tied bf16-rounded logits."""
+    rng = np.random.default_rng(5)
+    B, K, V = 200, 3, 16
+    zp = np.round(rng.normal(0, 1, (B, K + 1, V)) * 2) / 2    # many ties at the max
+    zq = zp.copy()
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok[::2] = zp[::2, :K].argmax(-1)                         # half the rows accept early
+    F = np.array([2, 2, 1, 1], dtype=np.int32)
+    g = orc.verify(zp.astype(np.float32), zq.astype(np.float32), tok, np.zeros(B, np.uint64), 0,
+                   F, 1.0, 0.0)
+    am = zp.argmax(-1)
+    for b in range(B):
+        k = next((i for i in range(K) if tok[b, i] != am[b, i]), K)
+        assert g["accept_len"][b] == k
+        assert g["bonus"][b] == am[b, k]
+
+
+def test_per_sequence_temperature_equals_separate_calls(orc):
+    """A temperature per sequence (0 = greedy) gives each sequence the
+    outputs of a call with that temperature alone (same Philox counters)."""
+    w = WORKLOADS["c1"]
+    bt = make_batch(w, B=6)
+    F = bt["fanout"]
+    Ts = np.array([1.0, 0.7, 0.0, 1.3, 0.0, 0.5])
+    tok = orc.draft_tokens(bt["draft"], F, w.C, 1.0, bt["seeds"], K=w.K)
+    both = orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], 4, F, w.C, Ts)
+    for b in range(6):
+        one = orc.verify(bt["target"][b:b + 1], bt["draft"][b:b + 1], tok[b:b + 1],
+                         bt["seeds"][b:b + 1], 4, F, w.C, Ts[b], row_ids=[b])
+        for key in ("accept_len", "bonus", "guesses"):
+            np.testing.assert_array_equal(both[key][b:b + 1], one[key])
+        np.testing.assert_allclose(both["resid_mass"][b], one["resid_mass"][0], rtol=0, atol=0)
+
+
 def test_bonus_law_monte_carlo(orc):
     """Given rejection at i the bonus follows normalize((p_i - q'_i)^+); given
     all accepted it follows p_K ([SD-7.3] §7.3.3).  Chi-square over 10^6
