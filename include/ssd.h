@@ -67,6 +67,8 @@ typedef enum {
 #define SSD_DEV_TIMEOUT 0x4        /* a bounded wait gave up; outputs are undefined */
 #define SSD_DEV_TABLE_FULL 0x8     /* cache insert found no free slot */
 #define SSD_DEV_DUPLICATE_KEY 0x10 /* cache insert met an existing key */
+#define SSD_DEV_BAD_TEMPERATURE 0x20 /* a per-sequence temperature negative or not
+                                        finite; that sequence is verified greedily */
 
 typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 
@@ -107,6 +109,11 @@ int ssd_version(void);
  *   guesses[b,j,:] = top-(F_j + 1) of z_draft[b,j,:] minus x_j (j < K),
  *                    truncated to F_j, padded with -1 to Fmax.
  * C = 1 (or all F_j = 0) is plain speculative decoding, bit for bit.
+ * T = 0 is the greedy limit T -> 0 (a serving setting the pages do not
+ * treat): x_i is accepted iff it is the argmax of z_target[b,i,:] (ties to
+ * the lower index), the bonus is the argmax of target row k, resid_mass is
+ * 1, and guess_q is 1 for the draft argmax and 0 for other guesses; no
+ * uniform is drawn.
  *
  * target      [B, K+1, V] logits: row (b, i) is row b*(K+1)+i.
  * draft       [B, Kq, V] logits, Kq in {K, K+1}: row (b, j) is row b*Kq+j.
@@ -127,6 +134,7 @@ int ssd_version(void);
  * Fmax        >= max F_j when guesses is given.
  * workspace   device, 256-byte aligned, >= ssd_verify_workspace_size(B,K,Kq,V).
  * dev_status  device int32 (or NULL): SSD_DEV_* bits are OR-ed in.
+ * T           temperature, finite and >= 0 (0: greedy).
  * ------------------------------------------------------------------------- */
 size_t ssd_verify_workspace_size(int B, int K, int Kq, int V);
 ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,
@@ -152,6 +160,29 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
  * ------------------------------------------------------------------------- */
 ssd_status ssd_verify_ck(const ssd_logits* target, const ssd_logits* draft, int B, int K,
                          int Kq, int V, float T, const int32_t* draft_tokens,
+                         const uint64_t* seeds, uint32_t round, const int32_t* fanout,
+                         const float* C_pos, int32_t* accept_len, int32_t* bonus,
+                         float* resid_mass, int32_t* guesses, float* guess_q, int Fmax,
+                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ssd_verify_ex -- ssd_verify with a temperature per sequence and an
+ * optional Saguaro factor per draft position (the pages use one T and one C;
+ * a batch of requests with their own sampling settings needs both).
+ *
+ * As ssd_verify_ck, with sequence b verified at temperature T_rows[b]:
+ * T_rows[b] > 0 as ssd_verify at that T; T_rows[b] = 0 greedy (see
+ * ssd_verify).  A negative or non-finite T_rows[b] is verified greedily and
+ * sets SSD_DEV_BAD_TEMPERATURE.  A call whose T_rows are all equal to T > 0
+ * gives the results of ssd_verify_ck with T.
+ *
+ * T_rows  device [B] float.
+ * C_pos   HOST [K] float in (0, 1], or NULL for C = 1 at every position.
+ * Other arguments, errors and outputs: ssd_verify.
+ * ------------------------------------------------------------------------- */
+ssd_status ssd_verify_ex(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                         int Kq, int V, const float* T_rows, const int32_t* draft_tokens,
                          const uint64_t* seeds, uint32_t round, const int32_t* fanout,
                          const float* C_pos, int32_t* accept_len, int32_t* bonus,
                          float* resid_mass, int32_t* guesses, float* guess_q, int Fmax,

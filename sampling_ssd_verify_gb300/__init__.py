@@ -29,6 +29,7 @@ __all__ = [
     "SSDError", "build", "lib", "verify", "verify_host", "topf_bonus", "saguaro_sample",
     "cache_bytes", "cache_build", "cache_build_guesses", "cache_lookup", "fanout",
     "DEV_BAD_TOKEN", "DEV_ZERO_RESIDUAL", "DEV_TIMEOUT", "DEV_TABLE_FULL", "DEV_DUPLICATE_KEY",
+    "DEV_BAD_TEMPERATURE",
 ]
 
 DEV_BAD_TOKEN = 0x1
@@ -36,6 +37,7 @@ DEV_ZERO_RESIDUAL = 0x2
 DEV_TIMEOUT = 0x4
 DEV_TABLE_FULL = 0x8
 DEV_DUPLICATE_KEY = 0x10
+DEV_BAD_TEMPERATURE = 0x20
 
 SSD_BF16, SSD_F32 = 0, 1
 _lib = None
@@ -62,6 +64,8 @@ _SIGS = {
     "ssd_verify": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32, _vp,
                     ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "ssd_verify_ck": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32, _vp,
+                       _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
+    "ssd_verify_ex": ([_LP, _LP, _i, _i, _i, _i, _vp, _vp, _vp, ctypes.c_uint32, _vp,
                        _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "ssd_topf_workspace_size": ([_i, _i, _i], _sz),
     "ssd_topf_bonus": ([_LP, _i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, _vp, _vp, _vp, _sz,
@@ -178,7 +182,8 @@ def verify(target, draft, draft_tokens, seeds, round_, fanout=None, C=1.0, T=1.0
     target [B, K+1, V], draft [B, Kq, V] (bf16 or fp32, same dtype),
     draft_tokens int32 [B, K], seeds 64-bit [B], fanout: sequence of Kq ints.
     C: the Saguaro factor, or a sequence of K factors, one per draft position
-    (ssd_verify_ck).
+    (ssd_verify_ck).  T: the temperature (0: greedy), or one per sequence --
+    a device float32 tensor [B] or anything numpy reads (ssd_verify_ex).
     Returns a dict of device tensors: accept_len, bonus, resid_mass, guesses,
     guess_q (the optional ones only when requested).
     """
@@ -208,6 +213,24 @@ def verify(target, draft, draft_tokens, seeds, round_, fanout=None, C=1.0, T=1.0
         raise SSDError("invalid verify shape")
     ws = workspace if workspace is not None else _workspace(wsb, dev)
     tl, dl = _logits(target), _logits(draft)
+    if np.ndim(T) > 0:
+        Tr = T if hasattr(T, "is_cuda") else torch.as_tensor(np.asarray(T, dtype=np.float32),
+                                                              device=dev)
+        if Tr.shape != (B,) or Tr.dtype != torch.float32 or not Tr.is_cuda:
+            raise SSDError("per-sequence T must be float32 [B] on the device")
+        Tr = Tr.contiguous()
+        Cv = None if np.ndim(C) == 0 and float(C) == 1.0 else \
+            np.ascontiguousarray(np.broadcast_to(np.asarray(C, dtype=np.float32), (K,)))
+        st = L.ssd_verify_ex(ctypes.byref(tl), ctypes.byref(dl), B, K, Kq, V, _dev_ptr(Tr),
+                             _dev_ptr(_i32(draft_tokens)), _dev_ptr(_u64_seeds(seeds, dev)),
+                             int(round_) & 0xFFFFFFFF, F.ctypes.data_as(ctypes.c_void_p),
+                             None if Cv is None else Cv.ctypes.data_as(ctypes.c_void_p),
+                             _dev_ptr(o["accept_len"]), _dev_ptr(o["bonus"]),
+                             _dev_ptr(o.get("resid_mass")), _dev_ptr(o.get("guesses")),
+                             _dev_ptr(o.get("guess_q")), Fmax, _dev_ptr(ws), ws.numel(),
+                             _dev_ptr(dev_status), _stream(stream))
+        _check(st, "ssd_verify_ex")
+        return o
     if np.ndim(C) == 0:
         fn, c_arg, name = L.ssd_verify, float(C), "ssd_verify"
     else:

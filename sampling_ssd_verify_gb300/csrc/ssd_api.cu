@@ -153,7 +153,6 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   q.V = V;
   q.nsub = L.nsub;
   q.total_units = (int64_t)groups * L.nsub;
-  q.c = p.c;
   q.gp = p.gparams;
   q.rowres = p.rowres;
   q.rpg = rpg;
@@ -274,9 +273,12 @@ size_t ssd_saguaro_workspace_size(int R, int V) {
 
 namespace {
 
-// ssd_verify with a Saguaro factor per draft position (Cv[0..K-1], host).
+// ssd_verify with a Saguaro factor per draft position (Cv[0..K-1], host) and,
+// when T_rows (device [B]) is given, a temperature per sequence instead of T.
+// T = 0 is the greedy limit.
 ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,
-                       int V, float T, const int32_t* draft_tokens, const uint64_t* seeds,
+                       int V, float T, const float* T_rows, const int32_t* draft_tokens,
+                       const uint64_t* seeds,
                        uint32_t round, const int32_t* fanout, const float* Cv,
                        int32_t* accept_len, int32_t* bonus, float* resid_mass, int32_t* guesses,
                        float* guess_q, int Fmax, void* workspace, size_t workspace_bytes,
@@ -285,7 +287,8 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
     return SSD_ERR_INVALID_ARG;
   if (!logits_ok(target, V) || !logits_ok(draft, V) || target->dtype != draft->dtype)
     return SSD_ERR_INVALID_ARG;
-  if (!finite_pos(T) || Cv == nullptr) return SSD_ERR_INVALID_ARG;
+  if (T_rows == nullptr && !(std::isfinite(T) && T >= 0.f)) return SSD_ERR_INVALID_ARG;
+  if (Cv == nullptr) return SSD_ERR_INVALID_ARG;
   for (int j = 0; j < K; ++j)
     if (!std::isfinite(Cv[j]) || !(Cv[j] > 0.f) || Cv[j] > 1.f) return SSD_ERR_INVALID_ARG;
   if (!draft_tokens || !seeds || !accept_len || !bonus) return SSD_ERR_INVALID_ARG;
@@ -308,14 +311,20 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Common cm;
   WsLayout L;
-  ssd_status st = setup(target, draft, B, K, Kq, K + 1, Kq, V, T, workspace, workspace_bytes, s,
-                        cm, L);
+  // a greedy sequence's (unused) sums take T = 1
+  const bool greedy_all = T_rows == nullptr && T == 0.f;
+  ssd_status st = setup(target, draft, B, K, Kq, K + 1, Kq, V, T > 0.f ? T : 1.f, workspace,
+                        workspace_bytes, s, cm, L);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
   for (int j = 0; j <= SSD_MAX_K; ++j) {
     p.F[j] = F[j];
     p.C[j] = j < K ? Cv[j] : 1.f;
   }
+  p.T_rows = T_rows;
+  p.greedy_all = greedy_all ? 1 : 0;
+  p.bonus = bonus;
+  p.resid_mass = resid_mass;
   p.need_top = need_top ? 1 : 0;
   p.tokens = draft_tokens;
   p.tokK = K;
@@ -332,7 +341,10 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
   q.out_token = bonus;
   q.out_mass = resid_mass;
   q.status = dev_status;
-  return run_pass(cm, target->dtype, need_top ? topk_for(maxF) : 0, true, s);
+  // greedy sequences keep a one-entry list (the argmax) on their target rows
+  int topk = need_top ? topk_for(maxF) : 0;
+  if (T_rows != nullptr || greedy_all) topk = std::max(topk, 2);
+  return run_pass(cm, target->dtype, topk, true, s);
 }
 
 }  // namespace
@@ -348,7 +360,8 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
   if (K < 1 || K > SSD_MAX_K) return SSD_ERR_INVALID_ARG;
   float Cv[SSD_MAX_K];
   for (int j = 0; j < K; ++j) Cv[j] = C;
-  return verify_impl(target, draft, B, K, Kq, V, T, draft_tokens, seeds, round, fanout, Cv,
+  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, draft_tokens, seeds, round, fanout,
+                     Cv,
                      accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
                      workspace_bytes, dev_status, stream);
 }
@@ -361,8 +374,23 @@ ssd_status ssd_verify_ck(const ssd_logits* target, const ssd_logits* draft, int 
                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
                          void* stream) {
   if (K < 1 || K > SSD_MAX_K || C_pos == nullptr) return SSD_ERR_INVALID_ARG;
-  return verify_impl(target, draft, B, K, Kq, V, T, draft_tokens, seeds, round, fanout, C_pos,
-                     accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, draft_tokens, seeds, round, fanout,
+                     C_pos, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+                     workspace_bytes, dev_status, stream);
+}
+
+ssd_status ssd_verify_ex(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                         int Kq, int V, const float* T_rows, const int32_t* draft_tokens,
+                         const uint64_t* seeds, uint32_t round, const int32_t* fanout,
+                         const float* C_pos, int32_t* accept_len, int32_t* bonus,
+                         float* resid_mass, int32_t* guesses, float* guess_q, int Fmax,
+                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                         void* stream) {
+  if (K < 1 || K > SSD_MAX_K || T_rows == nullptr) return SSD_ERR_INVALID_ARG;
+  float Cv[SSD_MAX_K];
+  for (int j = 0; j < K; ++j) Cv[j] = C_pos ? C_pos[j] : 1.f;
+  return verify_impl(target, draft, B, K, Kq, V, 1.f, T_rows, draft_tokens, seeds, round, fanout,
+                     Cv, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
                      workspace_bytes, dev_status, stream);
 }
 

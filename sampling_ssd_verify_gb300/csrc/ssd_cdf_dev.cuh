@@ -134,7 +134,7 @@ __device__ __forceinline__ float weight_global(const CdfParams& p, const GroupPa
                                          26, y, gp.row_t)) ? Elem<DT>::load(rt, y) : 0.f;
   const float zd = (gp.use_d && SSD_CHK(in_range(ad, ad + Elem<DT>::kSize, p.d_lo, p.d_hi), p.dbg,
                                          27, y, gp.row_d)) ? Elem<DT>::load(rd, y) : 0.f;
-  return weight(gp, p.c, y, zt, zd);
+  return weight(gp, gp.c, y, zt, zd);
 }
 
 __device__ __forceinline__ double warp_incl_scan(double v) {
@@ -344,6 +344,7 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   };
   load_round(0);  // in flight together with the group's parameters
   const GroupParams gp = load_gp(p.gp + g);
+  if (no_draw(gp)) return;  // the group's epilogue wrote its outputs
   const int esz = Elem<DT>::kSize;
   const char* rt = gp.use_t ? row_ptr(p.tgt, gp.row_t, p.t_stride, esz) : nullptr;
   const char* rd = gp.use_d ? row_ptr(p.dft, gp.row_d, p.d_stride, esz) : nullptr;
@@ -433,7 +434,7 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
     if (gp.use_t) load16<DT>(p, rt, true, y0, e1, zt);
     if (gp.use_d) load16<DT>(p, rd, false, y0, e1, zd);
     int lastpos = -1;
-    weights16(gp, p.c, y0, e1, zt, zd, w);
+    weights16(gp, gp.c, y0, e1, zt, zd, w);
 #pragma unroll
     for (int k = 0; k < 16; ++k)
       if (w[k] > 0.f) lastpos = y0 + k;
@@ -510,7 +511,7 @@ __device__ __forceinline__ float unit_sum_k(const CdfParams& p, const GroupParam
     float sv = 0.f;
 #pragma unroll
     for (int e = 0; e < VEC; ++e)
-      sv += weight_k<KIND, HAS_S>(gp, p.c, ue0 + vi * VEC + e, KIND != kSaguaro ? zt[e] : 0.f,
+      sv += weight_k<KIND, HAS_S>(gp, gp.c, ue0 + vi * VEC + e, KIND != kSaguaro ? zt[e] : 0.f,
                                   KIND != kTarget ? zd[e] : 0.f);
     s += sv;
   }
@@ -594,7 +595,7 @@ __device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
   constexpr int ES = Elem<DT>::kSize;
   const int lane = threadIdx.x & 31;
   const int uu = u + warp;
-  if (uu >= un) return;
+  if (uu >= un || no_draw(gp)) return;
   const int e0 = u * kUnitB;
   const int e1 = min(p.V, un * kUnitB);
   Half ht, hd;
@@ -630,7 +631,7 @@ __device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
       if (y < ue1) {
         const float zt = gp.use_t ? fetch<DT>(ht, y, p, true, half) : 0.f;
         const float zd = gp.use_d ? fetch<DT>(hd, y, p, false, half) : 0.f;
-        s += weight(gp, p.c, y, zt, zd);
+        s += weight(gp, gp.c, y, zt, zd);
       }
     }
   }

@@ -66,8 +66,12 @@ struct GroupParams {
   float mc_d, scale_out, scale_in;  // q'(y) = exp2(fl(z*c - mc_d)) * (in S ? scale_in : scale_out)
   float theta;      // S = { y : z > theta or (z == theta and y <= itheta) }
   int itheta;
+  float c;          // log2(e) / T of the group
   double u;         // uniform of the draw
 };
+// A group whose outputs its epilogue already wrote (a greedy sequence): its
+// draw chunks do nothing.
+__host__ __device__ inline bool no_draw(const GroupParams& gp) { return !gp.use_t && !gp.use_d; }
 
 struct StreamParams {
   const void* tgt;
@@ -86,6 +90,10 @@ struct StreamParams {
   unsigned long long* chunk_ctr;
   uint32_t* row_cut;        // per row: ordered-float lower bound on its top-list cut (0: none)
   float c;                  // log2(e) / T
+  // Per-sequence temperature (device [B]) or null: then every sequence uses
+  // T, greedy when greedy_all.  T = 0 is the greedy limit.
+  const float* T_rows;
+  int greedy_all;
   float C[SSD_MAX_K + 1];   // Saguaro factor per draft position (a continuation draw: C[0])
   int F[SSD_MAX_K + 1];
   int need_top;             // draft rows keep a top list
@@ -96,6 +104,8 @@ struct StreamParams {
   int jpos;                 // Saguaro: continuation position
   int mode;
   int32_t* accept_len;
+  int32_t* bonus;           // written by the epilogue of a greedy sequence
+  float* resid_mass;
   int32_t* guesses;         // [groups, nd, Fmax]
   float* guess_q;
   int Fmax;
@@ -125,7 +135,6 @@ struct CdfParams {
   // shorter), taken group by group.
   int cu, cpg;
   int64_t nchunks;
-  float c;
   int mode;
   const GroupParams* gp;
   const RowResult* rowres;  // Saguaro: the branch row's top list

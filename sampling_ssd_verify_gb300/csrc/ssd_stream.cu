@@ -369,11 +369,83 @@ __device__ __forceinline__ void fold_partial(Acc<TOPK>& a, const RowPartial* pp,
   }
 }
 
-// ---- the sequence epilogue of ssd_verify (warp 0 of the finishing CTA) -----------------
-__device__ void verify_epilogue(const StreamParams& p, int64_t g) {
+// ---- per-sequence temperature -----------------------------------------------------------
+// A sequence is greedy (the limit T -> 0) when its temperature is 0 -- or
+// negative or not finite, which also sets SSD_DEV_BAD_TEMPERATURE.  A greedy
+// sequence's sums (unused) take T = 1.
+__device__ __forceinline__ bool seq_greedy(const StreamParams& p, int64_t g) {
+  if (p.T_rows == nullptr) return p.greedy_all != 0;
+  const float T = __ldg(p.T_rows + g);
+  return !(T > 0.f && T <= 3.402823466e38f);
+}
+
+// log2(e) / T rounded once from fp64, as the host computes the scale of a
+// single temperature (kept out of line: the fp64 division is long).
+__device__ __noinline__ float scale_of_temperature(float T) {
+  return (T > 0.f && T <= 3.402823466e38f) ? (float)(1.4426950408889634 / (double)T)
+                                           : 1.4426950408889634f;
+}
+
+// log2(e) / T of sequence g: the scale of every exponent of its rows.
+__device__ __forceinline__ float seq_scale(const StreamParams& p, int64_t g) {
+  if (p.T_rows == nullptr) return p.c;
+  return scale_of_temperature(__ldg(p.T_rows + g));
+}
+
+// Top-list entries row `row` (row jr of sequence g) needs: F_j + 1 on a draft
+// row that feeds guesses or a Saguaro set, 1 (its argmax) on a target row of
+// a greedy sequence, otherwise none.
+__device__ __forceinline__ int row_need(const StreamParams& p, int64_t g, int jr) {
+  if (jr < p.nt) return p.mode == kModeVerify && seq_greedy(p, g) ? 1 : 0;
+  const int F = p.F[jr - p.nt];
+  return (p.need_top && F > 0) ? F + 1 : 0;
+}
+
+// Greedy verification of sequence g (the limit T -> 0): x_i is accepted iff
+// it is the argmax of target row i (ties to the lower index); the bonus is
+// the argmax of the first rejected target row, or of row K when every draft
+// is accepted.  Nothing is left to draw.  Warp 0 of the finishing CTA.
+__device__ void greedy_epilogue(const StreamParams& p, int64_t g) {
   const int lane = threadIdx.x & 31;
   const int K = p.K;
-  const double c = (double)p.c;
+  bool acc = true;
+  if (lane < K) {
+    const RowResult* rt = p.rowres + g * p.rpg + lane;
+    acc = __ldcg(&rt->x) == __ldcg(&rt->ti[0]);
+  }
+  const unsigned rej = ~__ballot_sync(0xffffffffu, acc) & (K >= 32 ? 0xffffffffu : ((1u << K) - 1u));
+  const int k = rej ? __ffs(rej) - 1 : K;
+  if (lane != 0) return;
+  if (!SSD_CHK(g < p.B && k >= 0 && k <= K, p.dbg, 8, g, k)) return;
+  p.accept_len[g] = k;
+  p.bonus[g] = __ldcg(&p.rowres[g * p.rpg + k].ti[0]);
+  if (p.resid_mass) p.resid_mass[g] = 1.f;
+  if (p.T_rows != nullptr && p.status) {
+    const float T = __ldg(p.T_rows + g);
+    if (T != 0.f) atomicOr(p.status, SSD_DEV_BAD_TEMPERATURE);
+  }
+  GroupParams gp = {};
+  gp.use_t = 0;  // no draw
+  gp.use_d = 0;
+  gp.theta = kPosInf;
+  gp.itheta = -1;
+  p.gparams[g] = gp;
+  if (p.grp_ready) {
+    __threadfence();
+    flag_release(p.grp_ready + g);
+  }
+}
+
+// ---- the sequence epilogue of ssd_verify (warp 0 of the finishing CTA) -----------------
+__device__ void verify_epilogue(const StreamParams& p, int64_t g) {
+  if (seq_greedy(p, g)) {
+    greedy_epilogue(p, g);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int K = p.K;
+  const float cf = seq_scale(p, g);
+  const double c = (double)cf;
   bool acc = true;
   if (lane < K) {
     const RowResult* rt = p.rowres + g * p.rpg + lane;
@@ -389,7 +461,7 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
       double QS = 0.0;
       bool inS = false;
       for (int f = 0; f < F; ++f) {
-        QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), p.c, -__ldcg(&rd->mc)));
+        QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), cf, -__ldcg(&rd->mc)));
         inS |= __ldcg(&rd->ti[f]) == x;
       }
       QS /= sq;
@@ -426,7 +498,7 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
       if (Ck < 1.f && F > 0) {
         double QS = 0.0;
         for (int f = 0; f < F; ++f)
-          QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), p.c, -gp.mc_d));
+          QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), cf, -gp.mc_d));
         QS /= sq;
         const double gn = 1.0 / (1.0 - (1.0 - (double)Ck) * QS);
         scale_out = gn / sq;
@@ -443,6 +515,7 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
       gp.scale_out = gp.scale_in = 0.f;
     }
     gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)k, 1u, p.round);
+    gp.c = cf;
     p.gparams[g] = gp;
     if (p.grp_ready) {
       __threadfence();
@@ -453,6 +526,7 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
 
 // Saguaro continuation draw: parameters of q' for branch row g.
 __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResult& rr) {
+  const float cf = seq_scale(p, g);
   GroupParams gp;
   gp.k = 0;
   gp.use_t = 0;
@@ -470,7 +544,7 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
   const float C = p.C[0];
   if (C < 1.f && F > 0) {
     double QS = 0.0;
-    for (int f = 0; f < F; ++f) QS += (double)exp2f(fmaf(rr.tv[f], p.c, -rr.mc));
+    for (int f = 0; f < F; ++f) QS += (double)exp2f(fmaf(rr.tv[f], cf, -rr.mc));
     QS /= rr.s;
     const double gn = 1.0 / (1.0 - (1.0 - (double)C) * QS);
     scale_out = gn / rr.s;
@@ -481,6 +555,7 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
   gp.scale_out = (float)scale_out;
   gp.scale_in = (float)scale_in;
   gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)p.jpos, 2u, p.round);
+  gp.c = cf;
   p.gparams[g] = gp;
   if (p.grp_ready) {
     __threadfence();
@@ -527,6 +602,8 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
   if (lane == 0 && SSD_CHK(row < p.NR, p.dbg, 5, row, p.NR)) p.rowres[row] = rr;
   // bonus guesses: top-(F_j+1) minus the sampled token, truncated to F_j
   if (!is_t && p.guesses != nullptr && lane == 0) {
+    const bool greedy = p.mode == kModeVerify && seq_greedy(p, g);
+    const float cf = seq_scale(p, g);
     const int F = p.F[j];
     int n = 0;
     const int64_t o = (g * p.nd + j) * (int64_t)p.Fmax;
@@ -534,7 +611,9 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
       if (rr.ti[k] < 0 || rr.ti[k] == rr.x) continue;
       if (!SSD_CHK(o + n < (int64_t)p.B * p.nd * p.Fmax && n < p.Fmax, p.dbg, 7, o + n, n)) break;
       p.guesses[o + n] = rr.ti[k];
-      if (p.guess_q) p.guess_q[o + n] = (float)((double)exp2f(fmaf(rr.tv[k], p.c, -MC)) / rr.s);
+      if (p.guess_q)
+        p.guess_q[o + n] = greedy ? (rr.ti[k] == rr.ti[0] ? 1.f : 0.f)
+                                  : (float)((double)exp2f(fmaf(rr.tv[k], cf, -MC)) / rr.s);
       ++n;
     }
     for (; n < p.Fmax; ++n) {
@@ -747,7 +826,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     return;
   }
 
-  const float c = p.c;
   if (warp >= kEpilogueWarp) {
     // ---------------- epilogue: merge, publish, finalise ----------------
     for (int piece = warp - kEpilogueWarp;; piece += kEpilogueWarps) {
@@ -772,9 +850,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       chunk_geom(p, chunk, row, kch, pu0, pu1);
       const int64_t g = row / p.rpg;
       const int jr = (int)(row - g * p.rpg);
-      const bool is_t = jr < p.nt;
-      const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
-      const int need = top ? p.F[jr - p.nt] + 1 : 0;  // list entries the row needs
+      const float c = seq_scale(p, g);
+      const int need = TOPK > 0 ? row_need(p, g, jr) : 0;  // list entries the row needs
+      const bool top = need > 0;
       Acc<TOPK> b;
       b.reset();
       if (lane < kConsumerWarps) {
@@ -805,10 +883,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         // the chunk's R-th best logit bounds the row's cut: later chunks of
         // the row start from it
         if (top && lane == 0) {
-          const int F = p.F[jr - p.nt];
           float v = kNegInf;
 #pragma unroll
-          for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) v = k == F ? b.tv[k] : v;
+          for (int k = 0; k < (TOPK > 0 ? TOPK : 1); ++k) v = k == need - 1 ? b.tv[k] : v;
           if (v != kNegInf) atomicMax(p.row_cut + row, ord_float(v));
         }
       }
@@ -904,9 +981,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int kch = d.kch;
     const int jr = d.jr;
     const bool is_t = jr < p.nt;
-    const bool top = TOPK > 0 && !is_t && p.need_top && p.F[jr - p.nt] > 0;
+    (void)is_t;  // read by the bounds-checked build only
+    const int64_t g = row / p.rpg;
+    const float c = seq_scale(p, g);
+    const int need = TOPK > 0 ? row_need(p, g, jr) : 0;
+    const bool top = need > 0;
     a.reset();
-    wl.reset(top ? p.F[jr - p.nt] + 1 : 1);
+    wl.reset(top ? need : 1);
     // pruning bound for this row's top list: what earlier chunks of the row
     // established, then the CTA's warps' cuts
     float ccut = kNegInf;

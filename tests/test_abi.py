@@ -111,7 +111,7 @@ def test_verify_rejects_bad_arguments_on_the_host(L):
     assert _verify(L, Kq=6) == inv
     assert _verify(L, V=1) == inv
     assert _verify(L, V=1 << 24) == inv
-    assert _verify(L, T=0.0) == inv
+    assert _verify(L, T=0.0) == 5                            # greedy: valid, no workspace
     assert _verify(L, T=-1.0) == inv
     assert _verify(L, T=float("inf")) == inv
     assert _verify(L, T=float("nan")) == inv
@@ -155,6 +155,22 @@ def test_verify_ck_rejects_bad_factors_on_the_host(L):
     assert _verify_ck(L, [0.5, 0.5, 0.5, float("nan")]) == inv
     assert _verify_ck(L, [0.5, 0.5, 0.5, 0.5], K=0, Kq=0) == inv
     assert _verify_ck(L, [0.3, 0.5, 1.0, 0.7]) == 5
+
+
+def test_verify_ex_needs_its_temperatures(L):
+    """ssd_verify_ex takes a device temperature per sequence (its values are
+    checked on the device); a missing array or bad factors are argument
+    errors, and valid arguments get as far as the (missing) workspace."""
+    t, d = _fake(), _fake()
+    C = np.array([0.5, 0.5, 0.0, 0.5], dtype=np.float32)
+
+    def call(T_rows, Cp):
+        return L.ssd_verify_ex(ctypes.byref(t), ctypes.byref(d), 1, 4, 5, 32, T_rows, 0x20000,
+                               0x30000, 0, None, Cp, 0x40000, 0x50000, None, None, None, 1, None,
+                               0, None, None)
+    assert call(None, None) == 1
+    assert call(0x60000, C.ctypes.data_as(ctypes.c_void_p)) == 1
+    assert call(0x60000, None) == 5
 
 
 def test_other_entry_points_reject_bad_arguments(L):

@@ -209,6 +209,70 @@ def test_per_position_C_equal_entries_match_scalar(orc):
         np.testing.assert_array_equal(a[k], b[k])
 
 
+def _as_f32(a):
+    """Logit array as float32 (bf16 arrays hold the raw 16-bit patterns)."""
+    return (a.astype(np.uint32) << 16).view(np.float32) if a.dtype == np.uint16 else a
+
+
+@pytest.mark.parametrize("name,B,V,dtype", [("c3", 16, 128256, "bf16"),
+                                            ("c5", 12, 151936, "f32"),
+                                            ("c1", 500, 32, "f32")])
+def test_greedy_verify(orc, name, B, V, dtype):
+    """T = 0, the greedy limit: a draft is accepted iff it is the target
+    row's argmax (ties to the lower index) and the bonus is the argmax of the
+    first rejected target row.  Greedy drafts (the draft rows' argmax) and
+    sampled drafts, against the oracle, every output exact."""
+    torch, dev = torch_dev()
+    w = WORKLOADS[name]
+    bt = make_batch(w, B=B, V=V, dtype=dtype)
+    K = w.K
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tg, dg = upload(bt["target"], dtype), upload(bt["draft"], dtype)
+    greedy_tok = _as_f32(bt["draft"])[:, :K].argmax(-1).astype(np.int32)
+    sampled_tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=K, nthreads=16)
+    for tok in (greedy_tok, sampled_tok):
+        g = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 0, F, w.C, 0.0))
+        o = orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], 0, F, w.C, 0.0,
+                       Fmax=max(1, int(F.max())), nthreads=16)
+        for k in ("accept_len", "bonus", "guesses", "guess_q"):
+            np.testing.assert_array_equal(g[k], o[k].astype(g[k].dtype), err_msg=k)
+        np.testing.assert_array_equal(g["resid_mass"], 1.0)
+    assert 0 < g["accept_len"].mean() <= K
+
+
+def test_per_sequence_temperature(orc):
+    """ssd_verify_ex: one temperature per sequence, greedy ones among them,
+    against the oracle; a negative temperature is verified greedily and
+    reported."""
+    torch, dev = torch_dev()
+    w = WORKLOADS["c5"]
+    B, V = 16, 40000
+    bt = make_batch(w, B=B, V=V)
+    F = np.asarray(w.fanout, dtype=np.int32)
+    Ts = np.array([1.0, 0.0, 0.7, 1.3, 0.0, 0.5, 1.0, 2.0] * 2, dtype=np.float32)
+    tok = orc.draft_tokens(bt["draft"], F, w.C, 1.0, bt["seeds"], K=w.K, nthreads=16)
+    tg, dg = upload(bt["target"], "f32"), upload(bt["draft"], "f32")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for rnd in (0, 1):
+        g = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), rnd, F, w.C,
+                             torch.from_numpy(Ts).to(dev), dev_status=status))
+        o = orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], rnd, F, w.C,
+                       Ts.astype(np.float64), Fmax=max(1, int(F.max())), nthreads=16)
+        compare_verify(g, o, w.K)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    bad = Ts.copy()
+    bad[3] = -1.0
+    g = to_np(ssd.verify(tg, dg, i32(tok), seeds_t(bt["seeds"]), 0, F, w.C,
+                         torch.from_numpy(bad).to(dev), dev_status=status))
+    torch.cuda.synchronize()
+    assert int(status.item()) & ssd.DEV_BAD_TEMPERATURE
+    bad[3] = 0.0
+    o = orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], 0, F, w.C,
+                   bad.astype(np.float64), Fmax=max(1, int(F.max())), nthreads=16)
+    compare_verify(g, o, w.K)
+
+
 def test_bad_token_sets_status(orc):
     torch, dev = torch_dev()
     w = WORKLOADS["c1"]
