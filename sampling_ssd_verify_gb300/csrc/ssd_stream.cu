@@ -39,6 +39,7 @@ constexpr float kPosInf = INFINITY;
 template <int TOPK>
 struct alignas(16) PieceRed {
   long long chunk;  // the piece's chunk, -1: no more pieces
+  float c;          // log2(e) / T of the piece's sequence
   float m[kConsumerWarps];
   float hi[kConsumerWarps];
   float lo[kConsumerWarps];
@@ -437,14 +438,13 @@ __device__ void greedy_epilogue(const StreamParams& p, int64_t g) {
 }
 
 // ---- the sequence epilogue of ssd_verify (warp 0 of the finishing CTA) -----------------
-__device__ void verify_epilogue(const StreamParams& p, int64_t g) {
+__device__ void verify_epilogue(const StreamParams& p, int64_t g, float cf) {
   if (seq_greedy(p, g)) {
     greedy_epilogue(p, g);
     return;
   }
   const int lane = threadIdx.x & 31;
   const int K = p.K;
-  const float cf = seq_scale(p, g);
   const double c = (double)cf;
   bool acc = true;
   if (lane < K) {
@@ -525,8 +525,8 @@ __device__ void verify_epilogue(const StreamParams& p, int64_t g) {
 }
 
 // Saguaro continuation draw: parameters of q' for branch row g.
-__device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResult& rr) {
-  const float cf = seq_scale(p, g);
+__device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResult& rr,
+                                 float cf) {
   GroupParams gp;
   gp.k = 0;
   gp.use_t = 0;
@@ -565,8 +565,8 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
 
 // Finalise row `row` from the merged (M, MC, S, top list) held by warp 0.
 template <int DT, int TOPK>
-__device__ void finalize_row(const StreamParams& p, int64_t row, float M, float MC, float Shi,
-                             float Slo, const Acc<TOPK>& a, bool top) {
+__device__ void finalize_row(const StreamParams& p, int64_t row, float c, float M, float MC,
+                             float Shi, float Slo, const Acc<TOPK>& a, bool top) {
   const int lane = threadIdx.x & 31;
   const int64_t g = row / p.rpg;
   const int jr = (int)(row - g * p.rpg);
@@ -603,7 +603,6 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
   // bonus guesses: top-(F_j+1) minus the sampled token, truncated to F_j
   if (!is_t && p.guesses != nullptr && lane == 0) {
     const bool greedy = p.mode == kModeVerify && seq_greedy(p, g);
-    const float cf = seq_scale(p, g);
     const int F = p.F[j];
     int n = 0;
     const int64_t o = (g * p.nd + j) * (int64_t)p.Fmax;
@@ -613,7 +612,7 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
       p.guesses[o + n] = rr.ti[k];
       if (p.guess_q)
         p.guess_q[o + n] = greedy ? (rr.ti[k] == rr.ti[0] ? 1.f : 0.f)
-                                  : (float)((double)exp2f(fmaf(rr.tv[k], cf, -MC)) / rr.s);
+                                  : (float)((double)exp2f(fmaf(rr.tv[k], c, -MC)) / rr.s);
       ++n;
     }
     for (; n < p.Fmax; ++n) {
@@ -633,9 +632,9 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float M, float 
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   if (p.mode == kModeVerify) {
-    verify_epilogue(p, g);
+    verify_epilogue(p, g, c);
   } else if (lane == 0) {
-    saguaro_epilogue(p, g, rr);
+    saguaro_epilogue(p, g, rr, c);
   }
 }
 
@@ -666,7 +665,10 @@ struct PieceDesc {
   const char* rp;  // element 0 of the row
   int jr;          // row within its group
   int kch;         // chunk of the row
-  // a chunk of the draws: group g, units [u0, u1), the group's parameters
+  float c;         // log2(e) / T of the row's sequence
+  int need;        // top-list entries the row needs
+  // the row's group; for a chunk of the draws also its units [u0, u1) and
+  // the group's parameters
   int64_t g;
   int u0, u1;
   GroupParams gp;
@@ -791,8 +793,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         d.pu0 = pu0;
         d.pu1 = pu1;
         d.rp = rg.rp;
-        d.jr = (int)(row - (row / p.rpg) * p.rpg);
+        const int64_t g = row / p.rpg;
+        d.g = g;
+        d.jr = (int)(row - g * p.rpg);
         d.kch = k;
+        d.c = seq_scale(p, g);
+        d.need = TOPK > 0 ? row_need(p, g, d.jr) : 0;
         for (int64_t u = pu0, un = 0; u < pu1; u = un) {
           un = min(u + ups, pu1);
           const Stage st = stage_of<DT>(rg, p.V, u, un);
@@ -850,7 +856,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       chunk_geom(p, chunk, row, kch, pu0, pu1);
       const int64_t g = row / p.rpg;
       const int jr = (int)(row - g * p.rpg);
-      const float c = seq_scale(p, g);
+      const float c = R.c;
       const int need = TOPK > 0 ? row_need(p, g, jr) : 0;  // list entries the row needs
       const bool top = need > 0;
       Acc<TOPK> b;
@@ -876,7 +882,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (top) warp_topk_merge<TOPK>(b.tv, b.ti, need);
       }
       if (p.nch == 1) {
-        finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, b, top);
+        finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, b, top);
         continue;
       }
       if constexpr (TOPK > 0) {
@@ -918,7 +924,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if constexpr (TOPK > 0) {
         if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti, need);
       }
-      finalize_row<DT, TOPK>(p, row, M, MC, Shi, Slo, mrg, top);
+      finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, mrg, top);
     }
     return;
   }
@@ -982,10 +988,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int jr = d.jr;
     const bool is_t = jr < p.nt;
     (void)is_t;  // read by the bounds-checked build only
-    const int64_t g = row / p.rpg;
-    const float c = seq_scale(p, g);
-    const int need = TOPK > 0 ? row_need(p, g, jr) : 0;
-    const bool top = need > 0;
+    const float c = d.c;
+    const int need = d.need;
+    const bool top = TOPK > 0 && need > 0;
     a.reset();
     wl.reset(top ? need : 1);
     // pruning bound for this row's top list: what earlier chunks of the row
@@ -1127,7 +1132,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       R.m[warp] = M;
       R.hi[warp] = Shi;
       R.lo[warp] = Slo;
-      if (warp == 0) R.chunk = chunk;
+      if (warp == 0) {
+        R.chunk = chunk;
+        R.c = c;
+      }
     }
     if (lane < (TOPK > 0 ? TOPK : 1)) {
       R.tv[warp][lane] = (TOPK > 0 && top) ? wl.lv : kNegInf;
