@@ -420,6 +420,22 @@ def run_reference(args):
     }))
 
 
+def run_fanout_ablation(args):
+    """Hit rate of the geometric and the uniform guess allocation against
+    temperature, on the workload's shape (seeded synthetic rounds, library
+    calls only).  Prints one JSON line."""
+    from sampling_ssd_verify_gb300.ablation import fanout_ablation
+    from ssd_inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    budget = int(sum(w.fanout))
+    rows = fanout_ablation(w, (0.5, 0.7, 1.0, 1.3, 1.6, 2.0), budget, Cs=sorted({1.0, w.C}),
+                           rounds=4, B=args.batch or None, V=args.vocab or None)
+    print(json.dumps({"ablation": "fanout", "workload": w.name, "budget": budget,
+                      "B": args.batch or w.B, "V": args.vocab or w.V, "rounds": 4,
+                      "data": "synthetic", "rows": rows}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,7 +449,12 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ablation", choices=["fanout"], default=None,
+                    help="instead of the benchmark: geometric vs uniform fan-out hit rates")
     args = ap.parse_args()
+    if args.ablation == "fanout":
+        run_fanout_ablation(args)
+        return
     if args.impl == "reference":
         args.steps = 3 if args.steps is None else args.steps
         args.warmup = 1 if args.warmup is None else args.warmup

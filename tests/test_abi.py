@@ -205,3 +205,16 @@ def test_binding_fails_loudly_without_a_gpu():
     t = torch.zeros((1, 5, 32))
     with pytest.raises(ssd.SSDError):
         ssd.verify(t, t, torch.zeros((1, 4), dtype=torch.int32), np.zeros(1, np.uint64), 0)
+
+
+def test_uniform_fanout_allocation():
+    """The ablation's uniform allocation spends the budget, differs by at most
+    one between positions and gives the remainder to the lowest positions."""
+    from sampling_ssd_verify_gb300.ablation import uniform_fanout
+
+    for K in (1, 4, 8):
+        for budget in (0, 5, 12, 24, 31):
+            F = uniform_fanout(K, budget)
+            assert len(F) == K + 1 and F.sum() == budget
+            assert F.max() - F.min() <= 1
+            assert np.all(np.diff(F) <= 0)

@@ -273,6 +273,30 @@ def test_per_sequence_temperature(orc):
     compare_verify(g, o, w.K)
 
 
+def test_fanout_ablation_round_matches_oracle(orc):
+    """One round of the fan-out ablation harness (library calls: Saguaro
+    drafts, verify with guesses, cache build and lookup) against the oracle
+    composed the same way, for the geometric and the uniform allocation."""
+    from sampling_ssd_verify_gb300.ablation import round_hits, uniform_fanout
+
+    w = dataclasses.replace(WORKLOADS["c5"], B=64, V=8192)
+    for F in (ssd.fanout(w.K, 24), uniform_fanout(w.K, 24)):
+        res = round_hits(w, F, 0.5, 1.0, seed=7, rnd=1)
+        bt = res["batch"]
+        tok_o = orc.draft_tokens(bt["draft"], F, 0.5, 1.0, bt["seeds"], round_=1, K=w.K,
+                                 nthreads=16)
+        same_tok = (tok_o == res["tokens"]).all(axis=1)
+        assert same_tok.mean() > 0.95
+        o = orc.verify(bt["target"], bt["draft"], res["tokens"], bt["seeds"], 1, F, 0.5, 1.0,
+                       nthreads=16)
+        compare_verify({"accept_len": res["accept_len"], "bonus": res["bonus"],
+                        "guesses": res["guesses"]}, o, w.K)
+        same = (o["accept_len"] == res["accept_len"]) & (o["bonus"] == res["bonus"])
+        hit_o = np.array([o["bonus"][b] in o["guesses"][b, o["accept_len"][b]]
+                          for b in range(w.B)])
+        np.testing.assert_array_equal(res["hit"][same], hit_o[same])
+
+
 def test_bad_token_sets_status(orc):
     torch, dev = torch_dev()
     w = WORKLOADS["c1"]
