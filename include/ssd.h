@@ -190,6 +190,35 @@ ssd_status ssd_verify_ex(const ssd_logits* target, const ssd_logits* draft, int 
                          void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ssd_verify_round -- one SSD round in one launch: ssd_verify, the outcome
+ * cache of the round's guesses (ssd_cache_build_guesses) and its lookup with
+ * every sequence's outcome (ssd_cache_lookup).  [SSD-note] §"SSD 的核心思想":
+ * the drafter prepares a continuation per predicted outcome (k, t) and the
+ * round goes on at once when the real outcome was predicted; §"Saguaro 优化三":
+ * the batch proceeds without waiting only if every sequence hits.
+ *
+ * Arguments and outputs of ssd_verify (guesses is required), plus:
+ * table       device, 16-byte aligned, table_bytes >= ssd_cache_bytes(B*Kq*Fmax);
+ *             its previous content is discarded (the launch clears it before
+ *             inserting); afterwards it holds the round's guesses in the
+ *             format of ssd_cache_build_guesses, so ssd_cache_lookup can read
+ *             it.  Too small: SSD_ERR_TABLE_FULL.
+ * out_branch  device [B] int32 out: (b*Kq + k)*Fmax + f of the guess that
+ *             equals the outcome (k, t) = (accept_len[b], bonus[b]), or -1.
+ * all_hit     device int32 out (or NULL): 1 if every sequence hit, else 0.
+ * The results equal those of the three calls in sequence; outputs are
+ * undefined after SSD_DEV_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+ssd_status ssd_verify_round(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                            int Kq, int V, float T, const int32_t* draft_tokens,
+                            const uint64_t* seeds, uint32_t round, const int32_t* fanout, float C,
+                            int32_t* accept_len, int32_t* bonus, float* resid_mass,
+                            int32_t* guesses, float* guess_q, int Fmax, void* table,
+                            size_t table_bytes, int32_t* out_branch, int32_t* all_hit,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
  * ssd_verify_noalloc -- ssd_verify without a caller workspace.  The pages have
  * no counterpart: this is a deployment convenience.
  *

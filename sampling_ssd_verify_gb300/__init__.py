@@ -26,7 +26,8 @@ import numpy as np
 from . import _build
 
 __all__ = [
-    "SSDError", "build", "lib", "verify", "verify_host", "topf_bonus", "saguaro_sample",
+    "SSDError", "build", "lib", "verify", "verify_round", "verify_host", "topf_bonus",
+    "saguaro_sample",
     "cache_bytes", "cache_build", "cache_build_guesses", "cache_lookup", "fanout",
     "DEV_BAD_TOKEN", "DEV_ZERO_RESIDUAL", "DEV_TIMEOUT", "DEV_TABLE_FULL", "DEV_DUPLICATE_KEY",
     "DEV_BAD_TEMPERATURE",
@@ -67,6 +68,9 @@ _SIGS = {
                        _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "ssd_verify_ex": ([_LP, _LP, _i, _i, _i, _i, _vp, _vp, _vp, ctypes.c_uint32, _vp,
                        _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
+    "ssd_verify_round": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32,
+                          _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp,
+                          _vp, _sz, _vp, _vp], _i),
     "ssd_topf_workspace_size": ([_i, _i, _i], _sz),
     "ssd_topf_bonus": ([_LP, _i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, _vp, _vp, _vp, _sz,
                         _vp, _vp], _i),
@@ -246,6 +250,55 @@ def verify(target, draft, draft_tokens, seeds, round_, fanout=None, C=1.0, T=1.0
             _dev_ptr(o.get("guess_q")), Fmax, _dev_ptr(ws), ws.numel(),
             _dev_ptr(dev_status), _stream(stream))
     _check(st, name)
+    return o
+
+
+def verify_round(target, draft, draft_tokens, seeds, round_, fanout, C=1.0, T=1.0,
+                 guess_q=True, resid_mass=True, table=None, workspace=None, dev_status=None,
+                 stream=None, out=None):
+    """ssd_verify_round: verify, the round's outcome cache and its lookup in
+    one launch.  Returns verify's outputs (guesses always) plus ``branch``
+    [B] and ``all_hit`` [1] (device tensors) and the ``table`` used."""
+    torch = _torch()
+    B, K1, V = target.shape
+    K = K1 - 1
+    Kq = draft.shape[-2]
+    dev = target.device
+    F = np.ascontiguousarray(fanout, dtype=np.int32)
+    if len(F) != Kq:
+        raise SSDError("fanout must have Kq entries")
+    Fmax = max(1, int(F.max()))
+    o = out if out is not None else {}
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["bonus"] = torch.empty(B, dtype=torch.int32, device=dev)
+        if resid_mass:
+            o["resid_mass"] = torch.empty(B, dtype=torch.float32, device=dev)
+        o["guesses"] = torch.empty((B, Kq, Fmax), dtype=torch.int32, device=dev)
+        if guess_q:
+            o["guess_q"] = torch.empty((B, Kq, Fmax), dtype=torch.float32, device=dev)
+        o["branch"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["all_hit"] = torch.empty(1, dtype=torch.int32, device=dev)
+    if table is None:
+        table = o.get("table")
+    if table is None:
+        table = torch.empty(cache_bytes(B * Kq * Fmax), dtype=torch.uint8, device=dev)
+    o["table"] = table
+    L = lib()
+    wsb = L.ssd_verify_workspace_size(B, K, Kq, V)
+    if wsb == 0:
+        raise SSDError("invalid verify shape")
+    ws = workspace if workspace is not None else _workspace(wsb, dev)
+    tl, dl = _logits(target), _logits(draft)
+    st = L.ssd_verify_round(ctypes.byref(tl), ctypes.byref(dl), B, K, Kq, V, float(T),
+                            _dev_ptr(_i32(draft_tokens)), _dev_ptr(_u64_seeds(seeds, dev)),
+                            int(round_) & 0xFFFFFFFF, F.ctypes.data_as(ctypes.c_void_p), float(C),
+                            _dev_ptr(o["accept_len"]), _dev_ptr(o["bonus"]),
+                            _dev_ptr(o.get("resid_mass")), _dev_ptr(o["guesses"]),
+                            _dev_ptr(o.get("guess_q")), Fmax, _dev_ptr(table), table.numel(),
+                            _dev_ptr(o["branch"]), _dev_ptr(o["all_hit"]), _dev_ptr(ws), ws.numel(),
+                            _dev_ptr(dev_status), _stream(stream))
+    _check(st, "ssd_verify_round")
     return o
 
 

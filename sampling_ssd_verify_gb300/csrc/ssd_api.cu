@@ -273,12 +273,20 @@ size_t ssd_saguaro_workspace_size(int R, int V) {
 
 namespace {
 
-// ssd_verify with a Saguaro factor per draft position (Cv[0..K-1], host) and,
-// when T_rows (device [B]) is given, a temperature per sequence instead of T.
-// T = 0 is the greedy limit.
+// The outcome cache of a round built and probed in the verify launch.
+struct RoundArgs {
+  void* table;
+  size_t table_bytes;
+  int32_t* out_branch;
+  int32_t* all_hit;
+};
+
+// ssd_verify with a Saguaro factor per draft position (Cv[0..K-1], host),
+// when T_rows (device [B]) is given a temperature per sequence instead of T
+// (T = 0 is the greedy limit), and when ra is given the round's cache.
 ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B, int K, int Kq,
-                       int V, float T, const float* T_rows, const int32_t* draft_tokens,
-                       const uint64_t* seeds,
+                       int V, float T, const float* T_rows, const RoundArgs* ra,
+                       const int32_t* draft_tokens, const uint64_t* seeds,
                        uint32_t round, const int32_t* fanout, const float* Cv,
                        int32_t* accept_len, int32_t* bonus, float* resid_mass, int32_t* guesses,
                        float* guess_q, int Fmax, void* workspace, size_t workspace_bytes,
@@ -304,6 +312,13 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
     }
   }
   if (guesses && (Fmax < 1 || Fmax < maxF)) return SSD_ERR_INVALID_ARG;
+  int64_t cache_cap = 0;
+  if (ra != nullptr) {
+    if (!guesses || !ra->out_branch || !ra->table || ((uintptr_t)ra->table & 15) != 0)
+      return SSD_ERR_INVALID_ARG;
+    cache_cap = capacity_of(ra->table_bytes);
+    if (cache_cap < 2 * (int64_t)B * Kq * Fmax) return SSD_ERR_TABLE_FULL;
+  }
   // top lists are needed for the guesses and for every position that biases
   bool biased = false;
   for (int j = 0; j < K; ++j) biased |= Cv[j] < 1.f && F[j] > 0;
@@ -325,6 +340,15 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
   p.greedy_all = greedy_all ? 1 : 0;
   p.bonus = bonus;
   p.resid_mass = resid_mass;
+  if (ra != nullptr) {
+    p.rc.table = ra->table;
+    p.rc.cap = cache_cap;
+    p.rc.branch = ra->out_branch;
+    p.rc.all_hit = ra->all_hit;
+    p.rc.cnt = p.chunk_ctr + 1;
+    p.rc.cleared = reinterpret_cast<int*>(p.chunk_ctr + 2);
+    cm.cp.rc = p.rc;
+  }
   p.need_top = need_top ? 1 : 0;
   p.tokens = draft_tokens;
   p.tokK = K;
@@ -360,8 +384,8 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
   if (K < 1 || K > SSD_MAX_K) return SSD_ERR_INVALID_ARG;
   float Cv[SSD_MAX_K];
   for (int j = 0; j < K; ++j) Cv[j] = C;
-  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, draft_tokens, seeds, round, fanout,
-                     Cv,
+  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, nullptr, draft_tokens, seeds, round,
+                     fanout, Cv,
                      accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
                      workspace_bytes, dev_status, stream);
 }
@@ -374,8 +398,25 @@ ssd_status ssd_verify_ck(const ssd_logits* target, const ssd_logits* draft, int 
                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
                          void* stream) {
   if (K < 1 || K > SSD_MAX_K || C_pos == nullptr) return SSD_ERR_INVALID_ARG;
-  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, draft_tokens, seeds, round, fanout,
-                     C_pos, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, nullptr, draft_tokens, seeds, round,
+                     fanout, C_pos, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+                     workspace_bytes, dev_status, stream);
+}
+
+ssd_status ssd_verify_round(const ssd_logits* target, const ssd_logits* draft, int B, int K,
+                            int Kq, int V, float T, const int32_t* draft_tokens,
+                            const uint64_t* seeds, uint32_t round, const int32_t* fanout, float C,
+                            int32_t* accept_len, int32_t* bonus, float* resid_mass,
+                            int32_t* guesses, float* guess_q, int Fmax, void* table,
+                            size_t table_bytes, int32_t* out_branch, int32_t* all_hit,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            void* stream) {
+  if (K < 1 || K > SSD_MAX_K) return SSD_ERR_INVALID_ARG;
+  float Cv[SSD_MAX_K];
+  for (int j = 0; j < K; ++j) Cv[j] = C;
+  const RoundArgs ra{table, table_bytes, out_branch, all_hit};
+  return verify_impl(target, draft, B, K, Kq, V, T, nullptr, &ra, draft_tokens, seeds, round,
+                     fanout, Cv, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
                      workspace_bytes, dev_status, stream);
 }
 
@@ -389,8 +430,8 @@ ssd_status ssd_verify_ex(const ssd_logits* target, const ssd_logits* draft, int 
   if (K < 1 || K > SSD_MAX_K || T_rows == nullptr) return SSD_ERR_INVALID_ARG;
   float Cv[SSD_MAX_K];
   for (int j = 0; j < K; ++j) Cv[j] = C_pos ? C_pos[j] : 1.f;
-  return verify_impl(target, draft, B, K, Kq, V, 1.f, T_rows, draft_tokens, seeds, round, fanout,
-                     Cv, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
+  return verify_impl(target, draft, B, K, Kq, V, 1.f, T_rows, nullptr, draft_tokens, seeds, round,
+                     fanout, Cv, accept_len, bonus, resid_mass, guesses, guess_q, Fmax, workspace,
                      workspace_bytes, dev_status, stream);
 }
 

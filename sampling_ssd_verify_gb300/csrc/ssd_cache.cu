@@ -7,17 +7,15 @@
 // in the cache.  §"Saguaro 优化三：自适应回退策略": the batch proceeds without
 // waiting only when every sequence hits.
 //
-// Open-addressed hash table of 16-byte slots {u64 key, i32 value, pad}; the
-// key packs (row:32 | k:8 | t:24), the empty key is all ones.  Slot index =
-// SplitMix64 finaliser of the key (Steele, Lea & Flood, "Fast splittable
-// pseudorandom number generators", OOPSLA'14) modulo the power-of-two
-// capacity; linear probing bounded by the capacity.
+// Open-addressed hash table of 16-byte slots (ssd_cache_dev.cuh); here the
+// key packs (row:32 | k:8 | t:24) and the empty key is all ones.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <algorithm>
 
+#include "ssd_cache_dev.cuh"
 #include "ssd_device.cuh"
 #include "ssd_internal.cuh"
 
@@ -25,49 +23,10 @@ namespace ssd {
 
 namespace {
 
-constexpr unsigned long long kEmpty = ~0ull;
-
-struct alignas(16) Slot {
-  unsigned long long key;
-  int value;
-  int pad;
-};
-
-__device__ __forceinline__ unsigned long long pack_key(int row, int k, int t) {
-  return ((unsigned long long)(uint32_t)row << 32) | ((unsigned long long)(k & 0xFF) << 24) |
-         (unsigned long long)(t & 0xFFFFFF);
-}
-
-__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  return z ^ (z >> 31);
-}
-
-__device__ void insert(Slot* tab, int64_t cap, unsigned long long key, int value,
-                       int32_t* status) {
-  int64_t i = (int64_t)(mix64(key) & (unsigned long long)(cap - 1));
-  for (int64_t probe = 0; probe < cap; ++probe) {
-    const unsigned long long old = atomicCAS(&tab[i].key, kEmpty, key);
-    if (old == kEmpty) {
-      tab[i].value = value;
-      return;
-    }
-    if (old == key) {
-      if (status) atomicOr(status, SSD_DEV_DUPLICATE_KEY);
-      return;
-    }
-    i = (i + 1) & (cap - 1);
-  }
-  if (status) atomicOr(status, SSD_DEV_TABLE_FULL);
-}
-
 __global__ void clear_kernel(Slot* tab, int64_t cap) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < cap;
        i += (int64_t)gridDim.x * blockDim.x) {
-    tab[i].key = kEmpty;
-    tab[i].value = -1;
-    tab[i].pad = 0;
+    slot_clear(tab + i);
   }
 }
 
@@ -82,9 +41,9 @@ __global__ void insert_kernel(Slot* tab, int64_t cap, const int32_t* row, const 
       if (g < 0) continue;
       const int b = (int)(i / ((int64_t)Kq * Fmax));
       const int kk = (int)((i / Fmax) % Kq);
-      insert(tab, cap, pack_key(b, kk, g), (int)i, status);
+      cache_insert(tab, cap, pack_key(b, kk, g), (int)i, status);
     } else {
-      insert(tab, cap, pack_key(row[i], k[i], t[i]), branch[i], status);
+      cache_insert(tab, cap, pack_key(row[i], k[i], t[i]), branch[i], status);
     }
   }
 }
@@ -94,18 +53,7 @@ __global__ void lookup_kernel(const Slot* tab, int64_t cap, const int32_t* accep
                               int32_t* all_hit) {
   int ok = 1;
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    const unsigned long long key = pack_key(b, accept_len[b], bonus[b]);
-    int64_t i = (int64_t)(mix64(key) & (unsigned long long)(cap - 1));
-    int v = -1;
-    for (int64_t probe = 0; probe < cap; ++probe) {
-      const unsigned long long kk = tab[i].key;
-      if (kk == key) {
-        v = tab[i].value;
-        break;
-      }
-      if (kk == kEmpty) break;
-      i = (i + 1) & (cap - 1);
-    }
+    const int v = cache_find(tab, cap, pack_key(b, accept_len[b], bonus[b]));
     out_branch[b] = v;
     ok &= v >= 0;
   }

@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ssd_cache_dev.cuh"
 #include "ssd_device.cuh"
 #include "ssd_internal.cuh"
 
@@ -469,6 +470,9 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   if (lane != 0) return;
   if (!SSD_CHK(g < p.groups && t >= 0 && t < p.V, p.dbg, 25, g, t)) return;
   p.out_token[g] = t;
+  if (p.rc.table != nullptr)  // the round's cache: look the outcome (k, t) up
+    round_outcome(static_cast<const Slot*>(p.rc.table), p.rc.cap, g, gp.k, t, p.groups,
+                  p.rc.branch, p.rc.all_hit, p.rc.cnt);
   if (p.out_mass) p.out_mass[g] = (float)Zd;
   if (p.out_qprime) p.out_qprime[g] = (float)((double)wt / Zd);
   if (p.out_guess) {

@@ -99,21 +99,27 @@ __device__ __forceinline__ int flag_acquire(const int* f) {
   return v;
 }
 
-// Wait (bounded, like mbar_wait) until the flag is set; false on a timeout
-// or when the CTA has already met an error.  One thread.
-__device__ __forceinline__ bool flag_wait(const int* f, volatile int* s_err, int32_t* status) {
-  if (flag_acquire(f)) return true;
+// Wait (bounded, like mbar_wait) until the counter reaches `target`; false
+// on a timeout or when the CTA has already met an error.  One thread.
+__device__ __forceinline__ bool count_wait(const int* f, int target, volatile int* s_err,
+                                           int32_t* status) {
+  if (flag_acquire(f) >= target) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (*s_err) return false;
     __nanosleep(256);
-    if (flag_acquire(f)) return true;
+    if (flag_acquire(f) >= target) return true;
     if (global_ns() - t0 > kWaitLimitNs) {
       *s_err = 1;
       if (status) atomicOr(status, SSD_DEV_TIMEOUT);
       return false;
     }
   }
+}
+
+// Wait (bounded) until the flag is set.
+__device__ __forceinline__ bool flag_wait(const int* f, volatile int* s_err, int32_t* status) {
+  return count_wait(f, 1, s_err, status);
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).

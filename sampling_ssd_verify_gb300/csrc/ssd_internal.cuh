@@ -73,6 +73,20 @@ struct GroupParams {
 // draw chunks do nothing.
 __host__ __device__ inline bool no_draw(const GroupParams& gp) { return !gp.use_t && !gp.use_d; }
 
+// The outcome cache of one round built and probed inside the verify launch
+// (ssd_verify_round): each draft row's guesses are inserted as the row is
+// finalised, and each sequence looks its outcome up once its bonus is known.
+// The epilogue warps clear the table at the start of the launch; inserts
+// wait (bounded) until every CTA has cleared its slice.
+struct RoundCache {
+  void* table;               // Slot[cap] (ssd_cache_dev.cuh), or null: no cache
+  int64_t cap;
+  int32_t* branch;           // [B] out
+  int32_t* all_hit;          // out (or null)
+  unsigned long long* cnt;   // (finished sequences << 32) | hits, zeroed per call
+  int* cleared;              // epilogue warps done clearing, zeroed per call
+};
+
 struct StreamParams {
   const void* tgt;
   int64_t t_stride;
@@ -106,6 +120,7 @@ struct StreamParams {
   int32_t* accept_len;
   int32_t* bonus;           // written by the epilogue of a greedy sequence
   float* resid_mass;
+  RoundCache rc;
   int32_t* guesses;         // [groups, nd, Fmax]
   float* guess_q;
   int Fmax;
@@ -146,6 +161,7 @@ struct CdfParams {
   float* out_qprime;        // Saguaro: q'(x)
   int32_t* out_guess;       // Saguaro: [groups, F]
   int F;
+  RoundCache rc;
   int32_t* status;
   const char* t_lo;
   const char* t_hi;
@@ -183,12 +199,13 @@ inline WsLayout ws_layout(int groups, int rpg, int V, int nch) {
   L.NR = (int64_t)groups * rpg;
   L.nsub = (V + kUnitB - 1) / kUnitB;
   // counters: row arrivals [NR], group arrivals [groups], CDF arrivals
-  // [groups], row cuts [NR], group-ready flags [groups], then the 8-byte
-  // chunk counter
+  // [groups], row cuts [NR], group-ready flags [groups], then 8-byte
+  // counters: chunks, round-cache outcomes, round-cache clearing
   size_t ncnt = 2 * (size_t)L.NR + 3 * (size_t)groups;
   L.cnt_off = 0;
   L.ctr_off = (ncnt * sizeof(int) + 7) & ~(size_t)7;
-  L.cnt_bytes = align256(L.ctr_off + sizeof(unsigned long long));
+  // chunk counter, round-cache outcomes, round-cache clearing
+  L.cnt_bytes = align256(L.ctr_off + 3 * sizeof(unsigned long long));
   L.part_off = L.cnt_bytes;
   const size_t slots = nch > 1 ? (size_t)L.NR * nch : 1;
   L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));

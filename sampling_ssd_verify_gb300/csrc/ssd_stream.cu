@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ssd_cache_dev.cuh"
 #include "ssd_cdf_dev.cuh"
 #include "ssd_device.cuh"
 #include "ssd_internal.cuh"
@@ -370,6 +371,18 @@ __device__ __forceinline__ void fold_partial(Acc<TOPK>& a, const RowPartial* pp,
   }
 }
 
+// Warp roles: warps 0..kConsumerWarps-1 reduce staged data, warp
+// kConsumerWarps takes chunks from the global counter and issues their bulk
+// copies, and kEpilogueWarps epilogue warps (piece p to warp p mod
+// kEpilogueWarps) merge each piece's per-warp results and do all
+// global-memory epilogue work, so the consumer warps never wait for it.
+// Piece results pass through a queue of kPieceSlots shared-memory slots
+// guarded by mbarriers.
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;  // the first epilogue warp
+constexpr int kEpilogueWarps = 2;
+constexpr int kStreamThreads = (kConsumerWarps + 1 + kEpilogueWarps) * 32;
+
 // ---- per-sequence temperature -----------------------------------------------------------
 // A sequence is greedy (the limit T -> 0) when its temperature is 0 -- or
 // negative or not finite, which also sets SSD_DEV_BAD_TEMPERATURE.  A greedy
@@ -419,8 +432,12 @@ __device__ void greedy_epilogue(const StreamParams& p, int64_t g) {
   if (lane != 0) return;
   if (!SSD_CHK(g < p.B && k >= 0 && k <= K, p.dbg, 8, g, k)) return;
   p.accept_len[g] = k;
-  p.bonus[g] = __ldcg(&p.rowres[g * p.rpg + k].ti[0]);
+  const int t = __ldcg(&p.rowres[g * p.rpg + k].ti[0]);
+  p.bonus[g] = t;
   if (p.resid_mass) p.resid_mass[g] = 1.f;
+  if (p.rc.table != nullptr)  // the round's cache: look the outcome (k, t) up
+    round_outcome(static_cast<const Slot*>(p.rc.table), p.rc.cap, g, k, t, p.B, p.rc.branch,
+                  p.rc.all_hit, p.rc.cnt);
   if (p.T_rows != nullptr && p.status) {
     const float T = __ldg(p.T_rows + g);
     if (T != 0.f) atomicOr(p.status, SSD_DEV_BAD_TEMPERATURE);
@@ -566,7 +583,8 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
 // Finalise row `row` from the merged (M, MC, S, top list) held by warp 0.
 template <int DT, int TOPK>
 __device__ void finalize_row(const StreamParams& p, int64_t row, float c, float M, float MC,
-                             float Shi, float Slo, const Acc<TOPK>& a, bool top) {
+                             float Shi, float Slo, const Acc<TOPK>& a, bool top, bool* cleared,
+                             volatile int* s_err) {
   const int lane = threadIdx.x & 31;
   const int64_t g = row / p.rpg;
   const int jr = (int)(row - g * p.rpg);
@@ -621,6 +639,29 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float c, float 
       if (p.guess_q) p.guess_q[o + n] = 0.f;
     }
   }
+  if (!is_t && p.rc.table != nullptr && p.guesses != nullptr && p.F[j] > 0) {
+    // the round's cache: guess f of this row (entry f of the list, or f + 1
+    // once the drafted token is passed) -> key (sequence, position, guess),
+    // value its index in the guesses array; one lane per guess, after every
+    // CTA has cleared its slice of the table
+    const int F = p.F[j];
+    if (!*cleared) {
+      int ok = 0;
+      if (lane == 0)
+        ok = count_wait(p.rc.cleared, (int)gridDim.x * kEpilogueWarps, s_err, p.status);
+      *cleared = __shfl_sync(0xffffffffu, ok, 0) != 0;
+    }
+    int sx = kMaxTopK;
+    for (int k = F; k >= 0; --k)
+      if (rr.ti[k] == rr.x) sx = k;
+    if (*cleared && lane < F) {
+      const int e = lane < sx ? lane : lane + 1;
+      const int tok = e < kMaxTopK ? rr.ti[e] : -1;
+      if (tok >= 0)
+        cache_insert(static_cast<Slot*>(p.rc.table), p.rc.cap, pack_key((int)g, j, tok),
+                     (int)((g * p.nd + j) * p.Fmax + lane), p.status);
+    }
+  }
   if (p.mode == kModeTopF) return;
   // sequence arrival
   int last = 0;
@@ -638,17 +679,6 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float c, float 
   }
 }
 
-// Warp roles: warps 0..kConsumerWarps-1 reduce staged data, warp
-// kConsumerWarps takes chunks from the global counter and issues their bulk
-// copies, and kEpilogueWarps epilogue warps (piece p to warp p mod
-// kEpilogueWarps) merge each piece's per-warp results and do all
-// global-memory epilogue work, so the consumer warps never wait for it.
-// Piece results pass through a queue of kPieceSlots shared-memory slots
-// guarded by mbarriers.
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kEpilogueWarp = kConsumerWarps + 1;  // the first epilogue warp
-constexpr int kEpilogueWarps = 2;
-constexpr int kStreamThreads = (kConsumerWarps + 1 + kEpilogueWarps) * 32;
 constexpr int kPieceSlots = 4;
 static_assert(kPieceSlots % kEpilogueWarps == 0, "a slot belongs to one epilogue warp");
 // Chunk of each piece, written by the producer before the piece's first
@@ -748,7 +778,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           int64_t g;
           int u0, u1;
           cdf_chunk_geom(cq, c - nS, g, u0, u1);
-          if (!SSD_CHK(g < cq.groups, p.dbg, 20, g, cq.groups) ||
+          if (!(g >= 0 && g < cq.groups && u0 < u1) ||
               !flag_wait(p.grp_ready + g, &s_err, p.status)) {
             c = -1;
           } else {
@@ -834,6 +864,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
   if (warp >= kEpilogueWarp) {
     // ---------------- epilogue: merge, publish, finalise ----------------
+    bool cleared = true;  // the round's cache table is cleared (or there is none)
+    if (p.rc.table != nullptr) {
+      // clear this warp's share of the CTA's slice of the table before the
+      // first piece arrives; inserts wait until every share is done
+      const int64_t per = (p.rc.cap + gridDim.x - 1) / gridDim.x;
+      const int64_t s0 = (int64_t)blockIdx.x * per;
+      const int64_t s1 = min(p.rc.cap, s0 + per);
+      Slot* tab = static_cast<Slot*>(p.rc.table);
+      for (int64_t i = s0 + (warp - kEpilogueWarp) * 32 + lane; i < s1; i += kEpilogueWarps * 32)
+        slot_clear(tab + i);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(p.rc.cleared, 1);
+      }
+      cleared = false;
+    }
     for (int piece = warp - kEpilogueWarp;; piece += kEpilogueWarps) {
       const int slot = piece % kPieceSlots;
       if (!mbar_wait(pfull + slot, (piece / kPieceSlots) & 1, &s_err, p.status)) break;
@@ -882,7 +929,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (top) warp_topk_merge<TOPK>(b.tv, b.ti, need);
       }
       if (p.nch == 1) {
-        finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, b, top);
+        finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, b, top, &cleared, &s_err);
         continue;
       }
       if constexpr (TOPK > 0) {
@@ -924,7 +971,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if constexpr (TOPK > 0) {
         if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti, need);
       }
-      finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, mrg, top);
+      finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, mrg, top, &cleared, &s_err);
     }
     return;
   }

@@ -173,6 +173,27 @@ def test_verify_ex_needs_its_temperatures(L):
     assert call(0x60000, None) == 5
 
 
+def test_verify_round_checks_its_table(L):
+    """ssd_verify_round needs the guesses, an output for the branches and a
+    16-byte aligned table of at least ssd_cache_bytes(B*Kq*Fmax) bytes."""
+    t, d = _fake(), _fake()
+    F = np.array([3, 3, 2, 2, 2], dtype=np.int32)
+    Fp = F.ctypes.data_as(ctypes.c_void_p)
+    need = L.ssd_cache_bytes(1 * 5 * 3)
+
+    def call(guesses=0x60000, table=0x70000, tb=None, branch=0x80000):
+        return L.ssd_verify_round(ctypes.byref(t), ctypes.byref(d), 1, 4, 5, 32, 1.0, 0x20000,
+                                  0x30000, 0, Fp, 0.5, 0x40000, 0x50000, None, guesses, None, 3,
+                                  table, need if tb is None else tb, branch, None, None, 0, None,
+                                  None)
+    assert call(guesses=None) == 1
+    assert call(branch=None) == 1
+    assert call(table=None) == 1
+    assert call(table=0x70008) == 1
+    assert call(tb=need // 2) == 3
+    assert call() == 5   # valid, but no workspace
+
+
 def test_other_entry_points_reject_bad_arguments(L):
     d = _fake()
     F = np.array([1, 1], dtype=np.int32)

@@ -297,6 +297,46 @@ def test_fanout_ablation_round_matches_oracle(orc):
         np.testing.assert_array_equal(res["hit"][same], hit_o[same])
 
 
+@pytest.mark.parametrize("name,B,V,dtype,T", [("c5", 32, 151936, "f32", None),
+                                              ("c3", 16, 128256, "bf16", None),
+                                              ("c1", 64, 32, "f32", None),
+                                              ("c1", 1, 32, "f32", None),
+                                              ("c4", 32, 151936, "bf16", 0.0)],
+                         ids=["c5-shape", "c3-shape", "c1-shape", "c1-one-row", "c4-greedy"])
+def test_verify_round_equals_separate_calls(orc, name, B, V, dtype, T):
+    """ssd_verify_round (verify, the round's outcome cache and its lookup in
+    one launch) gives the outputs of ssd_verify, ssd_cache_build_guesses and
+    ssd_cache_lookup called in sequence, bit for bit, over consecutive rounds
+    on the same table (a round never sees the previous round's keys)."""
+    torch, dev = torch_dev()
+    w = WORKLOADS[name]
+    T = w.T if T is None else T
+    bt = make_batch(w, B=B, V=V, dtype=dtype)
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tg, dg = upload(bt["target"], dtype), upload(bt["draft"], dtype)
+    seeds = seeds_t(bt["seeds"])
+    table = None
+    hits = 0
+    for rnd in range(3):
+        tok = i32(orc.draft_tokens(bt["draft"], F, w.C, max(T, 0.5), bt["seeds"], round_=rnd,
+                                   K=w.K))
+        a = ssd.verify(tg, dg, tok, seeds, rnd, F, w.C, T)
+        look = ssd.cache_lookup(ssd.cache_build_guesses(a["guesses"]), a["accept_len"],
+                                a["bonus"])
+        r = ssd.verify_round(tg, dg, tok, seeds, rnd, F, w.C, T, table=table)
+        table = r["table"]
+        torch.cuda.synchronize()
+        for k in a:
+            np.testing.assert_array_equal(r[k].cpu().numpy(), a[k].cpu().numpy(), err_msg=k)
+        np.testing.assert_array_equal(r["branch"].cpu().numpy(), look["branch"].cpu().numpy())
+        assert int(r["all_hit"].item()) == int(look["all_hit"].item())
+        # the table holds the round's guesses in the cache format
+        again = ssd.cache_lookup(table, r["accept_len"], r["bonus"])
+        np.testing.assert_array_equal(again["branch"].cpu().numpy(), look["branch"].cpu().numpy())
+        hits += int((r["branch"] >= 0).sum().item())
+    assert hits > 0
+
+
 def test_bad_token_sets_status(orc):
     torch, dev = torch_dev()
     w = WORKLOADS["c1"]
