@@ -354,6 +354,17 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------------------------ oracle
+def oracle_round(orc, bt, tok, r, F, w, cores, rows):
+    """One round by the oracle, as the GPU step does it: verify, then the
+    outcome cache of the guesses probed with every sequence's outcome."""
+    ref = orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], r, F, w.C, w.T,
+                     nthreads=cores, row_ids=rows)
+    g = ref["guesses"]
+    b, k, f = np.nonzero(g >= 0)
+    branch = (b * g.shape[1] + k) * g.shape[2] + f
+    return orc.cache_lookup(b, k, g[b, k, f], branch, ref["accept_len"], ref["bonus"])
+
+
 def cpu_baseline(w, seconds, rows_per_call=None):
     """The CPU oracle, as it stands, on a bounded sample of the workload's
     rows (all host threads)."""
@@ -368,15 +379,14 @@ def cpu_baseline(w, seconds, rows_per_call=None):
     tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=w.K, nthreads=cores)
     done, t0 = 0, time.perf_counter()
     while True:
-        orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], done, F, w.C, w.T,
-                   nthreads=cores, row_ids=rows)
+        oracle_round(orc, bt, tok, done, F, w, cores, rows)
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds or done >= 1000:
             break
     return {"value": n * done / el, "unit": "rows/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.B} rows x {done} calls ({el:.1f} s), fp64 oracle, "
-                      f"{cores} threads"}
+            "sample": f"{n} of {w.B} rows x {done} rounds ({el:.1f} s), fp64 oracle verify "
+                      f"and outcome-cache lookup, {cores} threads"}
 
 
 def run_reference(args):
@@ -397,8 +407,7 @@ def run_reference(args):
     tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=w.K, nthreads=cores)
 
     def step(r):
-        orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], r, F, w.C, w.T, nthreads=cores,
-                   row_ids=rows)
+        oracle_round(orc, bt, tok, r, F, w, cores, rows)
 
     for s in range(args.warmup):
         step(s)
