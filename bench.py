@@ -164,6 +164,12 @@ def job_rows_per_s(rows_per_rank, world, seconds):
 
 
 # ------------------------------------------------------------------------------ ours
+def bt_rows(bb, w):
+    """The [R, V] branch logits of a K = 0 batch (uint16 bf16 bits or f32)."""
+    rows = bb["target"][:, 0, :]
+    return rows.view(np.int16) if w.dtype == "bf16" else rows
+
+
 def run_ours(args):
     import torch
     import torch.distributed as tdist
@@ -205,7 +211,25 @@ def run_ours(args):
     ev_v = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
 
-    def step(r, evs=None):
+    # The SSD cache-build workload adds the drafter's side of the round: every
+    # outer row's branches draw their next continuation token with Saguaro
+    # sampling, one call per continuation position over fresh branch logits.
+    branch = []
+    if w.branches:
+        R = B * w.branches
+        for j in range(w.cont_positions):
+            bb = make_batch(w, B=R, K=0, seed=w.seed + 100 + j)
+            rows = torch.from_numpy(np.ascontiguousarray(bt_rows(bb, w))).to(dev)
+            if w.dtype == "bf16":
+                rows = rows.view(torch.bfloat16)
+            bs = torch.from_numpy(bb["seeds"].view(np.int64)).to(dev)
+            bws = torch.empty(ssd.lib().ssd_saguaro_workspace_size(R, V), dtype=torch.uint8,
+                              device=dev)
+            branch.append((rows, bs, int(F[j]), {}, bws))
+    ev_s = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)] if branch else None
+
+    def step(r, evs=None, evs_s=None):
         # one SSD round in one launch: verify, the outcome cache of the guesses
         # and the lookup of every sequence's outcome
         if evs is not None:
@@ -213,6 +237,13 @@ def run_ours(args):
         ssd.verify_round(tg, dg, tok, seeds, r, F, w.C, w.T, table=table, workspace=ws, out=out)
         if evs is not None:
             evs[1].record(stream)
+        if branch:
+            if evs_s is not None:
+                evs_s[0].record(stream)
+            for j, (rows, bs, Fj, so, bws) in enumerate(branch):
+                ssd.saguaro_sample(rows, w.T, w.C, Fj, bs, j, r, out=so, workspace=bws)
+            if evs_s is not None:
+                evs_s[1].record(stream)
 
     look = out
 
@@ -230,7 +261,7 @@ def run_ours(args):
     wall0 = time.perf_counter()
     t0.record(stream)
     for s in range(args.steps):
-        step(1000 + s, ev_v[s])
+        step(1000 + s, ev_v[s], ev_s[s] if ev_s else None)
     t1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -245,6 +276,16 @@ def run_ours(args):
     alg = w.algorithmic_bytes()
     hbm_peak, peak_kind = peaks()
     achieved = alg / (verify_ms * 1e-3) / 1e9
+    saguaro = None
+    alg_step = alg
+    if branch:
+        s_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_s])) / len(branch)
+        s_alg = B * w.branches * V * w.elem_bytes
+        alg_step = alg + len(branch) * s_alg
+        saguaro = {"calls_per_step": len(branch), "rows": B * w.branches, "ms_per_call": s_ms,
+                   "algorithmic_bytes_per_call": s_alg,
+                   "gb_per_s": s_alg / (s_ms * 1e-3) / 1e9,
+                   "frac": s_alg / (s_ms * 1e-3) / 1e9 / hbm_peak}
 
     # round statistics (untimed): acceptance, cache hit rate, all-rows-hit fraction
     # alpha: accepted over attempted draft positions (a row that stops at n < K
@@ -279,9 +320,15 @@ def run_ours(args):
         dg_raw = dg.view(torch.int16) if w.dtype == "bf16" else dg
         ne = max(3, min(args.steps, args.e2e_steps))
 
+        hbr = [(rows.view(torch.int16) if w.dtype == "bf16" else rows,
+                rows.cpu().view(torch.int16 if w.dtype == "bf16" else torch.float32).pin_memory())
+               for rows, *_ in branch]
+
         def e2e_step(r):
             tg_raw.copy_(ht, non_blocking=True)
             dg_raw.copy_(hd, non_blocking=True)
+            for dev_rows, host_rows in hbr:
+                dev_rows.copy_(host_rows, non_blocking=True)
             tok.copy_(htok, non_blocking=True)
             seeds.copy_(hseed, non_blocking=True)
             step(r)
@@ -300,7 +347,8 @@ def run_ours(args):
             e2e_step(90_000 + s)
         e2e_s = max_over_ranks(time.perf_counter() - w0, tdist, dev)
         h2d = int(ht.numel() * ht.element_size() + hd.numel() * hd.element_size()
-                  + htok.numel() * 4 + hseed.numel() * 8)
+                  + htok.numel() * 4 + hseed.numel() * 8
+                  + sum(h.numel() * h.element_size() for _, h in hbr))
         d2h = int(sum(v.numel() * v.element_size() for v in res_host.values()))
         e2e = {"value": job_rows_per_s(B * ne, world, e2e_s), "unit": "rows/s",
                "h2d_bytes_per_step": h2d,
@@ -332,7 +380,8 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else
                              "inputs smaller than L2",
                        "positions_per_s": (K + 1) * B * world * args.steps / (ms * 1e-3),
-                       "logits_gb_per_s": alg * world * args.steps / (ms * 1e-3) / 1e9,
+                       "logits_gb_per_s": alg_step * world * args.steps / (ms * 1e-3) / 1e9,
+                       "saguaro_sampling": saguaro,
                        "accept_mean": acc_sum / nr, "alpha_measured": alpha, "hit_rate": h,
                        "all_hit_fraction": all_hits / nr, "h_pow_B": h ** B,
                        "wall_s_timed": wall},

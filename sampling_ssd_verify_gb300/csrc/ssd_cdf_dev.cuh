@@ -545,15 +545,31 @@ __device__ __forceinline__ void cdf_chunk_geom(const CdfParams& p, long long c, 
   u1 = min(u0 + p.cu, p.nsub);
 }
 
+// Layout of a draw stage in a ring slot of kStageBytes: a weight that reads
+// both rows gets half the slot for each (target run first); a weight that
+// reads one row gets the whole slot, so it takes twice the units per stage.
+struct DrawLayout {
+  int ups;    // units per stage
+  int cap;    // bytes of one row's run
+  int off_d;  // offset of the draft run
+};
+
+template <int DT>
+__device__ __forceinline__ DrawLayout draw_layout(const GroupParams& gp) {
+  const bool two = gp.use_t && gp.use_d;
+  const int cap = two ? kStageBytes / 2 : kStageBytes;
+  return DrawLayout{cap / (kUnitB * Elem<DT>::kSize), cap, two ? kStageBytes / 2 : 0};
+}
+
 // Bulk copies of units [u, un) of a group's target row rt and draft row rd
 // (null: not part of the weight) into one stage: the target run at dst, the
-// draft run at dst + half, each from its first 16-byte boundary to its last;
-// completion is counted on `bar`.  One thread.
+// draft run at dst + lay.off_d, each from its first 16-byte boundary to its
+// last; completion is counted on `bar`.  One thread.
 template <int DT>
 __device__ __forceinline__ void cdf_issue_stage(const CdfParams& p, const char* rt,
                                                 const char* rd, int u, int un,
-                                                unsigned char* dst, int half, uint64_t* bar,
-                                                volatile int* s_err) {
+                                                unsigned char* dst, const DrawLayout& lay,
+                                                uint64_t* bar, volatile int* s_err) {
   constexpr int ES = Elem<DT>::kSize;
   const int e0 = u * kUnitB;
   const int e1 = min(p.V, un * kUnitB);
@@ -573,41 +589,39 @@ __device__ __forceinline__ void cdf_issue_stage(const CdfParams& p, const char* 
     if (a1[h] > a0[h])
       srcok &= SSD_CHK(in_range(a0[h], a1[h], h == 0 ? p.t_lo : p.d_lo, h == 0 ? p.t_hi : p.d_hi),
                        p.dbg, 21, a0[h], h);
-  srcok &= SSD_CHK((un - u) * kUnitB * ES <= half, p.dbg, 28, un - u, half);
+  srcok &= SSD_CHK((un - u) * kUnitB * ES <= lay.cap, p.dbg, 28, un - u, lay.cap);
   if (bytes > 0 && !*s_err && srcok) {
     mbar_arrive_expect_tx(bar, bytes);
     for (int h = 0; h < 2; ++h)
       if (a1[h] > a0[h])
-        bulk_g2s(dst + h * half, reinterpret_cast<const void*>(a0[h]), (uint32_t)(a1[h] - a0[h]),
-                 bar);
+        bulk_g2s(dst + (h == 0 ? 0 : lay.off_d), reinterpret_cast<const void*>(a0[h]),
+                 (uint32_t)(a1[h] - a0[h]), bar);
   } else {
     mbar_arrive(bar);
   }
 }
 
 // The weight sums of units [u, un) of group g, staged by cdf_issue_stage at
-// `stage`: consumer warp `warp` takes unit u + warp, and its lane 0 stores
-// the sum.  Units whose elements are not all in shared memory, 16-byte
-// aligned (row ends, unaligned rows), read the missing ones from global
-// memory.
+// `stage`: consumer warp `warp` takes units u + warp, u + warp + 16, ...,
+// and its lane 0 stores each sum.  Units whose elements are not all in
+// shared memory, 16-byte aligned (row ends, unaligned rows), read the missing
+// ones from global memory.
 template <int DT>
 __device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
                                                   const GroupParams& gp, const char* rt,
                                                   const char* rd, int u, int un,
-                                                  const unsigned char* stage, int half,
-                                                  int warp) {
-  constexpr int ES = Elem<DT>::kSize;
-  const int lane = threadIdx.x & 31;
-  const int uu = u + warp;
-  if (uu >= un || no_draw(gp)) return;
+                                                  const unsigned char* stage,
+                                                  const DrawLayout& lay, int warp) {
+  if (u + warp >= un || no_draw(gp)) return;
   const int e0 = u * kUnitB;
   const int e1 = min(p.V, un * kUnitB);
   Half ht, hd;
+  constexpr int ES = Elem<DT>::kSize;
   for (int h = 0; h < 2; ++h) {
     Half& H = h == 0 ? ht : hd;
     const char* r = h == 0 ? rt : rd;
     H.row = r;
-    H.sm = reinterpret_cast<const char*>(stage + h * half);
+    H.sm = reinterpret_cast<const char*>(stage + (h == 0 ? 0 : lay.off_d));
     H.ei0 = H.ei1 = e0;
     if (r != nullptr) {
       const uintptr_t b0 = (uintptr_t)(r + (int64_t)e0 * ES);
@@ -620,29 +634,32 @@ __device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
       }
     }
   }
-  const int ue0 = uu * kUnitB;
-  const int ue1 = min(ue0 + kUnitB, p.V);
-  constexpr int VEC = Elem<DT>::kVec;
-  bool fast = ue1 - ue0 == kUnitB;
-  if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
-  if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
-  float s = 0.f;
-  if (fast) {
-    s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
-  } else {
-    for (int m = 0; m < kUnitB / 32; ++m) {
-      const int y = ue0 + lane + 32 * m;
-      if (y < ue1) {
-        const float zt = gp.use_t ? fetch<DT>(ht, y, p, true, half) : 0.f;
-        const float zd = gp.use_d ? fetch<DT>(hd, y, p, false, half) : 0.f;
-        s += weight(gp, gp.c, y, zt, zd);
+  const int lane = threadIdx.x & 31;
+  for (int uu = u + warp; uu < un; uu += kConsumerWarps) {
+    const int ue0 = uu * kUnitB;
+    const int ue1 = min(ue0 + kUnitB, p.V);
+    constexpr int VEC = Elem<DT>::kVec;
+    bool fast = ue1 - ue0 == kUnitB;
+    if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
+    if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
+    float s = 0.f;
+    if (fast) {
+      s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
+    } else {
+      for (int m = 0; m < kUnitB / 32; ++m) {
+        const int y = ue0 + lane + 32 * m;
+        if (y < ue1) {
+          const float zt = gp.use_t ? fetch<DT>(ht, y, p, true, lay.cap) : 0.f;
+          const float zd = gp.use_d ? fetch<DT>(hd, y, p, false, lay.cap) : 0.f;
+          s += weight(gp, gp.c, y, zt, zd);
+        }
       }
     }
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
-    p.subsum[g * p.nsub + uu] = s;
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
+      p.subsum[g * p.nsub + uu] = s;
+  }
 }
 
 // A finished chunk of group g (nu units, their sums stored): count it into

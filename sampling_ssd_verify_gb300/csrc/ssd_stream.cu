@@ -721,7 +721,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const CdfParams& cq = vp.q;  // the draws (cq.nchunks == 0: none)
   const long long nS = p.nchunks;
   const long long ntot = nS + cq.nchunks;
-  constexpr int kUps = fused_units_per_stage(Elem<DT>::kSize);  // units of a draw stage
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesA * kStageBytes);
@@ -804,12 +803,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           constexpr int ES = Elem<DT>::kSize;
           const char* rt = d.gp.use_t ? row_ptr(cq.tgt, d.gp.row_t, cq.t_stride, ES) : nullptr;
           const char* rd = d.gp.use_d ? row_ptr(cq.dft, d.gp.row_d, cq.d_stride, ES) : nullptr;
+          const DrawLayout lay = draw_layout<DT>(d.gp);
           for (int u = d.u0, un = 0; u < d.u1; u = un) {
-            un = min(u + kUps, d.u1);
+            un = min(u + lay.ups, d.u1);
             const int slot = n % kStagesA;
             if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
-            cdf_issue_stage<DT>(cq, rt, rd, u, un, ring + slot * kStageBytes, kStageBytes / 2,
-                                full + slot, &s_err);
+            cdf_issue_stage<DT>(cq, rt, rd, u, un, ring + slot * kStageBytes, lay, full + slot,
+                                &s_err);
             ++n;
           }
           continue;
@@ -1009,11 +1009,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       constexpr int ES = Elem<DT>::kSize;
       const char* rt = gp.use_t ? row_ptr(cq.tgt, gp.row_t, cq.t_stride, ES) : nullptr;
       const char* rd = gp.use_d ? row_ptr(cq.dft, gp.row_d, cq.d_stride, ES) : nullptr;
+      const DrawLayout lay = draw_layout<DT>(gp);
       for (int u = u0, un = 0; u < u1; u = un) {
-        un = min(u + kUps, u1);
+        un = min(u + lay.ups, u1);
         if (u != u0) mbar_wait(full + slot, phase, &s_err, p.status);
-        cdf_consume_stage<DT>(cq, g, gp, rt, rd, u, un, ring + slot * kStageBytes,
-                              kStageBytes / 2, warp);
+        cdf_consume_stage<DT>(cq, g, gp, rt, rd, u, un, ring + slot * kStageBytes, lay, warp);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + slot);
         if (++slot == kStagesA) {
