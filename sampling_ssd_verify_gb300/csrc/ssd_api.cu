@@ -96,10 +96,10 @@ struct Common {
 // rpg = nt + nd rows.
 ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, int K, int Kq,
                  int nt, int nd, int V, float T, void* workspace, size_t ws_bytes,
-                 cudaStream_t stream, Common& cm, WsLayout& L) {
+                 cudaStream_t stream, Common& cm, WsLayout& L, bool usum = false) {
   const int rpg = nt + nd;
   L = ws_layout(groups, rpg, V,
-                stream_chunks_per_row((int64_t)groups * rpg, units_per_row(V)));
+                stream_chunks_per_row((int64_t)groups * rpg, units_per_row(V)), usum);
   if (workspace == nullptr || ((uintptr_t)workspace & 255) != 0 || ws_bytes < L.total)
     return SSD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -131,6 +131,11 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.partials = reinterpret_cast<RowPartial*>(ws + L.part_off);
   p.rowres = reinterpret_cast<RowResult*>(ws + L.rowres_off);
   p.gparams = reinterpret_cast<GroupParams*>(ws + L.gp_off);
+  if (usum) {
+    p.usum = reinterpret_cast<float2*>(ws + L.usum_off);
+    const int su = 32 * (16 / esize_of(draft->dtype));  // 32 vectors of 16 bytes
+    p.nsu = (V + su - 1) / su;
+  }
   const int es = esize_of(draft->dtype);
   if (target != nullptr) {
     p.t_lo = static_cast<const char*>(target->ptr);
@@ -266,7 +271,7 @@ size_t ssd_topf_workspace_size(int B, int Kq, int V) {
 
 size_t ssd_saguaro_workspace_size(int R, int V) {
   if (R < 1 || V < 2 || V > SSD_MAX_V) return 0;
-  return ws_layout(R, 1, V, stream_chunks_per_row((int64_t)R, units_per_row(V))).total;
+  return ws_layout(R, 1, V, stream_chunks_per_row((int64_t)R, units_per_row(V)), true).total;
 }
 
 }  // extern "C"
@@ -483,7 +488,14 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Common cm;
   WsLayout L;
-  ssd_status st = setup(nullptr, draft, R, 0, 1, 0, 1, V, T, workspace, workspace_bytes, s, cm, L);
+  // Aligned rows of whole 16-byte vectors: the streaming pass writes the
+  // sub-unit sums the draw needs, and each row draws as soon as it is done,
+  // without reading the row again.
+  const int es = esize_of(draft->dtype);
+  const bool direct = ((uintptr_t)draft->ptr % 16) == 0 && (draft->row_stride * es) % 16 == 0 &&
+                      (V * es) % 16 == 0;
+  ssd_status st = setup(nullptr, draft, R, 0, 1, 0, 1, V, T, workspace, workspace_bytes, s, cm, L,
+                        direct);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
   p.F[0] = F;
@@ -502,7 +514,7 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
   q.out_guess = F > 0 ? out_guess : nullptr;
   q.F = F;
   q.status = dev_status;
-  return run_pass(cm, draft->dtype, need_top ? topk_for(F) : 0, true, s);
+  return run_pass(cm, draft->dtype, need_top ? topk_for(F) : 0, !direct, s);
 }
 
 size_t ssd_cache_bytes(int n_keys) {

@@ -128,6 +128,11 @@ struct StreamParams {
   int* grp_cnt;
   int* grp_ready;           // per group: 1 once its draw parameters are published
   RowPartial* partials;     // slot row * nch + chunk of row
+  // One-row draws whose unit sums the streaming pass writes (Saguaro rows,
+  // aligned): per 32-vector sub-unit of each row, (sum of exp2(z*c - off),
+  // off); null when the draws read the rows again.
+  float2* usum;
+  int nsu;                  // sub-units per row
   RowResult* rowres;
   GroupParams* gparams;
   int32_t* status;
@@ -184,7 +189,7 @@ struct VerifyParams {
 struct WsLayout {
   size_t cnt_off, cnt_bytes;       // counters (cleared each call)
   size_t ctr_off;                  // the chunk counter, within the counters
-  size_t part_off, rowres_off, gp_off, sub_off, dbg_off, total;
+  size_t part_off, rowres_off, gp_off, sub_off, usum_off, dbg_off, total;
   int64_t NR;
   int groups, nsub;
 };
@@ -192,8 +197,9 @@ struct WsLayout {
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // nch: chunks per row of the streaming pass; split rows (nch > 1) need one
-// partial slot per chunk.
-inline WsLayout ws_layout(int groups, int rpg, int V, int nch) {
+// partial slot per chunk.  usum: room for the streaming pass's sub-unit sums
+// of every row (sub-units of at least 128 elements).
+inline WsLayout ws_layout(int groups, int rpg, int V, int nch, bool usum = false) {
   WsLayout L;
   L.groups = groups;
   L.NR = (int64_t)groups * rpg;
@@ -211,7 +217,9 @@ inline WsLayout ws_layout(int groups, int rpg, int V, int nch) {
   L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));
   L.gp_off = L.rowres_off + align256((size_t)L.NR * sizeof(RowResult));
   L.sub_off = L.gp_off + align256((size_t)groups * sizeof(GroupParams));
-  L.dbg_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));
+  L.usum_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));
+  const size_t usum_bytes = usum ? (size_t)L.NR * ((V + 127) / 128) * 2 * sizeof(float) : 0;
+  L.dbg_off = L.usum_off + align256(usum_bytes);
   L.total = L.dbg_off + 256;  // bounds-check record of SSD_CHECKS builds
   return L;
 }

@@ -214,7 +214,56 @@ struct SAcc {
     }
     add(e[0]);
   }
+  // As take<N> for NV vectors of N / NV logits each, also returning each
+  // vector's sum (at this thread's offset mc after the call); the thread's
+  // total is the sum of the vector sums.
+  template <int N, int NV>
+  __device__ __forceinline__ void take_split(const float* x, float vm, float c, float* vs) {
+    constexpr int W = N / NV;
+    if (vm > m) raise_max(vm, c);
+    float e[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(x[k], c, -mc));
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      float* v = e + q * W;
+#pragma unroll
+      for (int w = W / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) v[k] += v[k + w];
+      vs[q] = v[0];
+    }
+    float t[NV];
+#pragma unroll
+    for (int q = 0; q < NV; ++q) t[q] = vs[q];
+#pragma unroll
+    for (int w = NV / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int q = 0; q < w; ++q) t[q] += t[q + w];
+    add(t[0]);
+  }
 };
+
+// The warp's sums of NV sub-units (one 32-vector run each, lane l holding
+// vector l's sum vs[q] at its own offset mc): rescaled to the warp's largest
+// offset and stored with it as (sum, offset) for sub-units su0 + q * step of
+// row `row`.  Called by all 32 lanes.
+template <int NV>
+__device__ __forceinline__ void store_subunits(const StreamParams& p, int64_t row, int su0,
+                                               int step, const float* vs, float mc) {
+  const int lane = threadIdx.x & 31;
+  const float mcw = unord_float(__reduce_max_sync(0xffffffffu, ord_float(mc)));
+  const float sc = (mc == -INFINITY || mcw == -INFINITY) ? 0.f : ex2(mc - mcw);
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    float v = vs[q] * sc;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    const int su = su0 + q * step;
+    if (lane == 0 && SSD_CHK(su < p.nsu && row < p.NR, p.dbg, 11, su, row))
+      p.usum[row * p.nsu + su] = make_float2(v, mcw);
+  }
+}
 
 // One warp-wide top list: lane l < TOPK holds the l-th best candidate by
 // (logit desc, index asc); (cv, ci) is the TOPK-th entry, known to all lanes.
@@ -580,11 +629,44 @@ __device__ void saguaro_epilogue(const StreamParams& p, int64_t g, const RowResu
   }
 }
 
+// The unit sums of a Saguaro row's draw weight q'(y), from the sub-unit sums
+// the streaming pass wrote: each sub-unit rescaled from its offset to the
+// row's, times the weight outside the cached set S, plus the difference of
+// the weights for the tokens of S (the top F of the row).  One warp; the
+// row's draw parameters are published by lane 0 before.
+template <int DT>
+__device__ void saguaro_unit_sums(const StreamParams& p, const CdfParams& cq, int64_t g,
+                                  const RowResult& rr, float c) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kSpu = kUnitB / (32 * Elem<DT>::kVec);  // sub-units per unit
+  const GroupParams gp = load_gp(cq.gp + g);
+  const float2* us = p.usum + g * p.nsu;
+  const int F = gp.theta != kPosInf ? p.F[0] : 0;
+  for (int u = lane; u < cq.nsub; u += 32) {
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kSpu; ++k) {
+      const int su = u * kSpu + k;
+      if (su < p.nsu) {
+        const float2 v = __ldcg(us + su);
+        if (v.x > 0.f) sum += v.x * ex2(v.y - gp.mc_d);
+      }
+    }
+    float w = sum * gp.scale_out;
+    for (int f = 0; f < F; ++f)
+      if (rr.ti[f] >= 0 && rr.ti[f] / kUnitB == u)
+        w += (gp.scale_in - gp.scale_out) * ex2(fmaf(rr.tv[f], c, -gp.mc_d));
+    if (SSD_CHK(g < cq.groups && u < cq.nsub, p.dbg, 12, g, u))
+      cq.subsum[g * cq.nsub + u] = fmaxf(w, 0.f);
+  }
+  __syncwarp();
+}
+
 // Finalise row `row` from the merged (M, MC, S, top list) held by warp 0.
 template <int DT, int TOPK>
-__device__ void finalize_row(const StreamParams& p, int64_t row, float c, float M, float MC,
-                             float Shi, float Slo, const Acc<TOPK>& a, bool top, bool* cleared,
-                             volatile int* s_err) {
+__device__ void finalize_row(const StreamParams& p, const CdfParams& cq, int64_t row, float c,
+                             float M, float MC, float Shi, float Slo, const Acc<TOPK>& a,
+                             bool top, bool* cleared, volatile int* s_err) {
   const int lane = threadIdx.x & 31;
   const int64_t g = row / p.rpg;
   const int jr = (int)(row - g * p.rpg);
@@ -674,8 +756,14 @@ __device__ void finalize_row(const StreamParams& p, int64_t row, float c, float 
   if (!last) return;
   if (p.mode == kModeVerify) {
     verify_epilogue(p, g, c);
-  } else if (lane == 0) {
-    saguaro_epilogue(p, g, rr, c);
+  } else {
+    if (lane == 0) saguaro_epilogue(p, g, rr, c);
+    if (p.usum != nullptr) {
+      // the row's unit sums from the streaming pass, then its draw
+      __syncwarp();
+      saguaro_unit_sums<DT>(p, cq, g, rr, c);
+      group_draw<DT>(cq, g);
+    }
   }
 }
 
@@ -929,7 +1017,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (top) warp_topk_merge<TOPK>(b.tv, b.ti, need);
       }
       if (p.nch == 1) {
-        finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, b, top, &cleared, &s_err);
+        finalize_row<DT, TOPK>(p, cq, row, c, M, MC, Shi, Slo, b, top, &cleared, &s_err);
         continue;
       }
       if constexpr (TOPK > 0) {
@@ -971,7 +1059,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if constexpr (TOPK > 0) {
         if (top) warp_topk_merge<TOPK>(mrg.tv, mrg.ti, need);
       }
-      finalize_row<DT, TOPK>(p, row, c, M, MC, Shi, Slo, mrg, top, &cleared, &s_err);
+      finalize_row<DT, TOPK>(p, cq, row, c, M, MC, Shi, Slo, mrg, top, &cleared, &s_err);
     }
     return;
   }
@@ -1079,7 +1167,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         float vm = vq[0];
 #pragma unroll
         for (int q = 1; q < kVpt; ++q) vm = fmaxf(vm, vq[q]);
-        a.take<N>(x, vm, c);
+        if (p.usum != nullptr) {
+          // the sums of the warp's four 32-vector runs, for the row's draw
+          float vs[kVpt];
+          a.take_split<N, kVpt>(x, vm, c, vs);
+          store_subunits<kVpt>(p, row, ei0 / (32 * VEC) + warp, kConsumerWarps, vs, a.mc);
+        } else {
+          a.take<N>(x, vm, c);
+        }
         if (TOPK > 0 && top) {
           if (!booted) {
             // First full stage of the piece: bound the row's R-th best by the
@@ -1104,14 +1199,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           float vm = kNegInf;
           uint4 rv = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
           if (DT == 1) rv = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+          float vs1 = 0.f;
           if (v < nvec && SSD_CHK(v < kVecs, p.dbg, 10, v, nvec)) {
             rv = sv[v];
             Elem<DT>::unpack(rv, x);
             vm = x[0];
 #pragma unroll
             for (int k = 1; k < VEC; ++k) vm = fmaxf(vm, x[k]);
-            a.take<VEC>(x, vm, c);
+            if (p.usum != nullptr)
+              a.take_split<VEC, 1>(x, vm, c, &vs1);
+            else
+              a.take<VEC>(x, vm, c);
           }
+          if (p.usum != nullptr) store_subunits<1>(p, row, (ei0 + v0 * VEC) / (32 * VEC), 0, &vs1, a.mc);
           if (TOPK > 0 && top) wl.template offer<DT, 1>(&rv, &vm, vm, ei0 + v * VEC, 0, ccut);
         }
       }
