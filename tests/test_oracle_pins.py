@@ -220,6 +220,41 @@ def test_losslessness_exact_enumeration(orc, V, K, C, T):
         assert abs(reach[i + 1] / reach[i] - alpha) < 1e-12
 
 
+def test_losslessness_with_a_factor_per_position(orc):
+    """Losslessness does not depend on C being shared by the positions: with a
+    different Saguaro factor at every draft position ([SSD-note] §"关于逐位置 C
+    的思考") the emitted token at every position still follows p_j exactly, and
+    the acceptance of position i is sum min(p_i, q'_i(C_i))."""
+    rng = np.random.default_rng(77)
+    V, K, T = 6, 3, 1.0
+    zp = rng.normal(0, 2, (K + 1, V))
+    zq = zp + rng.normal(0, 1, (K + 1, V))
+    F = [2, 2, 1, 1]
+    Cs = (0.2, 0.7, 0.4)
+    p = [orc.softmax(zp[i], T) for i in range(K + 1)]
+    qp = [orc.saguaro_dist(zq[j], T, F[j], Cs[j]) for j in range(K)]
+    law = np.zeros((K + 1, V))
+    reach = np.zeros(K + 1)
+    resid = []
+    for i in range(K):
+        w, Z = orc.residual(p[i], qp[i])
+        resid.append(w / Z)
+    for xs in itertools.product(range(V), repeat=K):
+        alive = np.prod([qp[j][xs[j]] for j in range(K)])
+        for i in range(K):
+            reach[i] += alive
+            a = orc.accept_prob(p[i][xs[i]], qp[i][xs[i]])
+            law[i, xs[i]] += alive * a
+            law[i] += alive * (1 - a) * resid[i]
+            alive *= a
+        reach[K] += alive
+        law[K] += alive * p[K]
+    for j in range(K + 1):
+        np.testing.assert_allclose(law[j] / reach[j], p[j], rtol=0, atol=1e-12)
+    for i in range(K):
+        assert abs(reach[i + 1] / reach[i] - np.minimum(p[i], qp[i]).sum()) < 1e-12
+
+
 def test_losslessness_enumeration_detects_wrong_accept_rule(orc):
     """The enumeration pin is sensitive: composing the same steps with an
     inverted ratio min(1, q/p) breaks losslessness."""
