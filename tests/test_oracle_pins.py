@@ -383,6 +383,9 @@ def test_greedy_is_the_low_temperature_limit(orc):
                             0.005)
             np.testing.assert_array_equal(g["accept_len"], s_["accept_len"])
             np.testing.assert_array_equal(g["bonus"], s_["bonus"])
+            # the guesses' draft probabilities tend to 1 for the argmax, 0 otherwise
+            np.testing.assert_array_equal(g["guesses"], s_["guesses"])
+            np.testing.assert_allclose(g["guess_q"], s_["guess_q"], rtol=0, atol=1e-12)
     assert 0 < g["accept_len"].mean() < K
     np.testing.assert_array_equal(g["resid_mass"], 1.0)
 
@@ -418,7 +421,7 @@ def test_per_sequence_temperature_equals_separate_calls(orc):
     for b in range(6):
         one = orc.verify(bt["target"][b:b + 1], bt["draft"][b:b + 1], tok[b:b + 1],
                          bt["seeds"][b:b + 1], 4, F, w.C, Ts[b], row_ids=[b])
-        for key in ("accept_len", "bonus", "guesses"):
+        for key in ("accept_len", "bonus", "guesses", "guess_q"):
             np.testing.assert_array_equal(both[key][b:b + 1], one[key])
         np.testing.assert_allclose(both["resid_mass"][b], one["resid_mass"][0], rtol=0, atol=0)
 
