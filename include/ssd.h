@@ -281,6 +281,9 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
  *   guesses = top-(F+1) of z[r,:] minus x, truncated to F.
  *
  * draft       [R, V] logits.
+ * T           temperature, finite and > 0.
+ * C           Saguaro factor in (0, 1] (the factor of position j when the
+ *             caller uses one per position).
  * F           cached-set size / guesses per row, 0..SSD_MAX_F.
  * seeds       device [R] uint64.   j: continuation position (counter word).
  * out_token   device [R] int32 out.
