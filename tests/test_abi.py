@@ -34,6 +34,24 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_is_plain_c(tmp_path, lang, std):
+    """ssd.h is a C ABI: it compiles as strict C99 and as C++ (no torch or
+    C++-only types in the declarations)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") if lang == "c" else shutil.which("g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cpp")
+    src.write_text('#include "ssd.h"\nint main(void) { return ssd_version() < 0; }\n')
+    r = subprocess.run([cc, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.dirname(HEADER), "-fsyntax-only", str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
