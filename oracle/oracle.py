@@ -75,8 +75,17 @@ def _configure(L):
                                  ctypes.c_int, _i32p, ctypes.c_int, _i32p, _dp, ctypes.c_int]
     L.orc_saguaro_sample.argtypes = [_vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_double, ctypes.c_double,
-                                     ctypes.c_int, _u64p, ctypes.c_int, ctypes.c_uint32,
+                                     ctypes.c_int, _i32p, _u64p, ctypes.c_int, ctypes.c_uint32,
                                      _i32p, _dp, _i32p, _dp, ctypes.c_int, _i32p]
+    L.orc_tree_verify.argtypes = [_vp, _vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                  _i32p, _i32p, _u64p, ctypes.c_uint32, _i32p, _i32p,
+                                  ctypes.c_int, _i32p, _dp, _dp, _dp, ctypes.c_int]
+    L.orc_tree_verify.restype = ctypes.c_int
+    L.orc_tree_draft.argtypes = [_vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_double, _i32p, _u64p, ctypes.c_uint32,
+                                 _i32p, ctypes.c_int]
+    L.orc_tree_draft.restype = ctypes.c_int
     L.orc_cache_lookup.argtypes = [_i32p, _i32p, _i32p, _i32p, ctypes.c_int, _i32p, _i32p,
                                    ctypes.c_int, _i32p, _i32p]
     L.orc_cache_lookup.restype = ctypes.c_int
@@ -279,19 +288,79 @@ def topf_bonus(draft, F, T, tokens=None, K=0, Fmax=None, nthreads=1):
 
 
 def saguaro_sample(rows, T, C, F, seeds, j, round_, nthreads=1, row_ids=None):
-    """rows [R, V] (uint16 bf16 bits or float32)."""
+    """rows [R, V] (uint16 bf16 bits or float32); F one fan-out for every row
+    or one per row (guesses then have max(F) columns, -1 padded)."""
     rows = np.ascontiguousarray(rows)
     R, V = rows.shape
     seeds = np.ascontiguousarray(seeds, dtype=np.uint64)
+    if np.ndim(F) == 0:
+        Fc, Fr = int(F), None
+    else:
+        Fr = _i32(F)
+        if Fr.shape != (R,):
+            raise ValueError("per-row F must have R entries")
+        Fc = int(Fr.max()) if R else 0
     tok = np.zeros(R, dtype=np.int32)
     qp = np.zeros(R)
-    g = np.zeros((R, max(F, 1)), dtype=np.int32)
+    g = np.zeros((R, max(Fc, 1)), dtype=np.int32)
     mc = np.zeros(R)
     lib().orc_saguaro_sample(rows.ctypes.data, _dtype_code(rows), V, R, V, float(T), float(C),
-                             int(F), _p(seeds, _u64p), int(j), int(round_), _p(tok, _i32p),
-                             _p(qp, _dp), _p(g, _i32p), _p(mc, _dp), int(nthreads),
-                             _p(None if row_ids is None else _i32(row_ids), _i32p))
-    return dict(token=tok, qprime=qp, guesses=g[:, :F], margin_cdf=mc)
+                             Fc, _p(Fr, _i32p), _p(seeds, _u64p), int(j), int(round_),
+                             _p(tok, _i32p), _p(qp, _dp), _p(g, _i32p), _p(mc, _dp),
+                             int(nthreads), _p(None if row_ids is None else _i32(row_ids), _i32p))
+    return dict(token=tok, qprime=qp, guesses=g[:, :Fc], margin_cdf=mc)
+
+
+def tree_depth(parent):
+    """Depth of the deepest node of a tree given by parent[] (root 0)."""
+    parent = _i32(parent)
+    d = np.zeros(len(parent), dtype=np.int64)
+    for u in range(1, len(parent)):
+        d[u] = d[parent[u]] + 1
+    return int(d.max()) if len(d) else 0
+
+
+def tree_verify(target, draft, parent, tokens, seeds, round_, T, nthreads=1):
+    """target, draft [B, N, V] (uint16 bf16 bits or float32): row u of a tree
+    is p_u / q_u at node u; parent [N] (parent[0] = -1); tokens [B, N]."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    B, N, V = target.shape
+    parent = _i32(parent)
+    tokens = _i32(tokens).reshape(B, N)
+    seeds = np.ascontiguousarray(seeds, dtype=np.uint64)
+    Dmax = max(1, tree_depth(parent))
+    acc = np.zeros(B, dtype=np.int32)
+    path = np.zeros((B, Dmax), dtype=np.int32)
+    bon = np.zeros(B, dtype=np.int32)
+    Z = np.zeros(B)
+    ma = np.zeros(B)
+    mc = np.zeros(B)
+    rc = lib().orc_tree_verify(target.ctypes.data, draft.ctypes.data, _dtype_code(target), V, V,
+                               B, N, V, float(T), _p(parent, _i32p), _p(tokens, _i32p),
+                               _p(seeds, _u64p), int(round_), _p(acc, _i32p), _p(path, _i32p),
+                               Dmax, _p(bon, _i32p), _p(Z, _dp), _p(ma, _dp), _p(mc, _dp),
+                               int(nthreads))
+    if rc == 3:
+        raise ValueError("parent[] is not a tree with parent[u] < u")
+    if rc:
+        raise ValueError("draft token outside [0, V)")
+    return dict(accept_len=acc, path=path, bonus=bon, resid_mass=Z, margin_accept=ma,
+                margin_cdf=mc)
+
+
+def tree_draft(draft, parent, seeds, round_, T, nthreads=1):
+    """Draft tokens [B, N] of a tree: x_v ~ q_{parent(v)} (entry 0 is -1)."""
+    draft = np.ascontiguousarray(draft)
+    B, N, V = draft.shape
+    parent = _i32(parent)
+    seeds = np.ascontiguousarray(seeds, dtype=np.uint64)
+    tok = np.zeros((B, N), dtype=np.int32)
+    if lib().orc_tree_draft(draft.ctypes.data, _dtype_code(draft), V, B, N, V, float(T),
+                            _p(parent, _i32p), _p(seeds, _u64p), int(round_), _p(tok, _i32p),
+                            int(nthreads)):
+        raise ValueError("parent[] is not a tree with parent[u] < u")
+    return tok
 
 
 def cache_lookup(row, k, t, branch, accept_len, bonus):

@@ -443,19 +443,23 @@ int orc_topf_bonus(const void* draft, int dtype, int64_t d_stride, int B, int Kq
 }
 
 // ---- a6: Saguaro continuation sampling -------------------------------------
-// For each branch row r: S = top-F of the row's draft logits; x ~ q' by
-// inverse CDF at u = U(seed_r; r, j, 2, round); guesses = top-(F+1) minus x,
-// truncated to F.  [SSD-note] §"Saguaro 优化二" and §"实现细节：缓存怎么建"
-// (all branches' continuations are drafted as one batch).
+// For each branch row r: S = top-F_r of the row's draft logits; x ~ q' by
+// inverse CDF at u = U(seed_r; r, j, 2, round); guesses = top-(F_r+1) minus x,
+// truncated to F_r.  [SSD-note] §"Saguaro 优化二" and §"实现细节：缓存怎么建"
+// (all branches' continuations are drafted as one batch).  A branch row's
+// fan-out is that of the outcome position it continues (§"最优扇出度分配"),
+// so F_rows (or NULL: F for every row) gives one per row; out_guess has F
+// columns (F >= every F_r), padded with -1.
 int orc_saguaro_sample(const void* draft, int dtype, int64_t stride, int R, int V, double T,
-                       double C, int F, const uint64_t* seeds, int j, uint32_t round,
-                       int32_t* out_token, double* out_qprime, int32_t* out_guess,
+                       double C, int F, const int32_t* F_rows, const uint64_t* seeds, int j,
+                       uint32_t round, int32_t* out_token, double* out_qprime, int32_t* out_guess,
                        double* margin_cdf, int nthreads, const int32_t* row_ids) {
   parallel_rows(R, nthreads, [&](int r) {
+    const int Fr = F_rows ? F_rows[r] : F;
     auto z = load_row(draft, dtype, (int64_t)r * stride, V);
     auto q = softmax(z, T);
-    auto top1 = top_n(z, F + 1);
-    std::vector<int> S(top1.begin(), top1.begin() + std::min<int>(F, top1.size()));
+    auto top1 = top_n(z, Fr + 1);
+    std::vector<int> S(top1.begin(), top1.begin() + std::min<int>(Fr, top1.size()));
     auto qp = saguaro(q, S, C);
     double Z = 0.0;
     for (double v : qp) Z += v;
@@ -467,8 +471,111 @@ int orc_saguaro_sample(const void* draft, int dtype, int64_t stride, int R, int 
     if (out_qprime) out_qprime[r] = qp[x];
     if (margin_cdf) margin_cdf[r] = m;
     if (out_guess) {
-      auto g = guesses_from(top1, F, x);
+      auto g = guesses_from(top1, Fr, x);
       for (int f = 0; f < F; ++f) out_guess[(int64_t)r * F + f] = f < (int)g.size() ? g[f] : -1;
+    }
+  });
+  return 0;
+}
+
+// ---- tree drafts ------------------------------------------------------------
+// [SD-7.3] §7.3.9 item 3 names tree-shaped drafts (树形草稿: several candidate
+// continuations per position instead of one chain) as the next step.  The
+// pages give no algorithm; the reading taken is multi-candidate rejection
+// sampling with recursive residuals, the plain generalisation of the
+// per-token rule of §7.3.3 to several candidates:
+//   * a tree of N nodes shared by the batch: parent[0] = -1 (node 0 is the
+//     last verified position), 0 <= parent[u] < u; node u >= 1 holds draft
+//     token x_u, drawn from q_{parent(u)}, the draft distribution at its
+//     parent; the children of a node are tried in increasing index order;
+//   * target row u is p_u (the target distribution after node u's path),
+//     draft row u is q_u;
+//   * at node u with current residual r (r = p_u on arrival), child v is
+//     accepted with probability min(1, r(x_v) / q_u(x_v)) (uniform
+//     U(seed_b; b, v-1, 0, round)); accepted: move to v with r = p_v;
+//     rejected: r = (r - q_u)^+ / sum (r - q_u)^+ and try the next child;
+//   * no child accepted (or u is a leaf): the bonus t ~ r by inverse CDF at
+//     U(seed_b; b, u, 1, round).
+// A chain (every node has one child) is the linear verification with C = 1,
+// uniform for uniform.  Outputs: accept_len = depth of the final node, path
+// = the accepted nodes (-1 padded to Dmax), bonus, resid_mass = the mass of
+// the last residual step (the sum of p_u, about 1, when the final node
+// rejected nothing).
+int orc_tree_verify(const void* target, const void* draft, int dtype, int64_t t_stride,
+                    int64_t d_stride, int B, int N, int V, double T, const int32_t* parent,
+                    const int32_t* tokens, const uint64_t* seeds, uint32_t round,
+                    int32_t* accept_len, int32_t* path, int Dmax, int32_t* bonus,
+                    double* resid_mass, double* margin_accept, double* margin_cdf,
+                    int nthreads) {
+  for (int u = 1; u < N; ++u)
+    if (parent[u] < 0 || parent[u] >= u) return 3;
+  for (int64_t i = 0; i < (int64_t)B * N; ++i)
+    if (i % N != 0 && (tokens[i] < 0 || tokens[i] >= V)) return 1;
+  parallel_rows(B, nthreads, [&](int b) {
+    const int32_t* x = tokens + (int64_t)b * N;
+    int u = 0, depth = 0;
+    double mA = INFINITY;
+    std::vector<double> r = softmax(load_row(target, dtype, ((int64_t)b * N) * t_stride, V), T);
+    double Zlast = -1.0;
+    for (int d = 0; d < Dmax; ++d) path[(int64_t)b * Dmax + d] = -1;
+    while (true) {
+      std::vector<double> q;
+      bool moved = false;
+      Zlast = -1.0;  // no rejection at this node yet
+      for (int v = u + 1; v < N && !moved; ++v) {
+        if (parent[v] != u) continue;
+        if (q.empty())
+          q = softmax(load_row(draft, dtype, ((int64_t)b * N + u) * d_stride, V), T);
+        const double ratio = q[x[v]] > 0.0 ? r[x[v]] / q[x[v]] : INFINITY;
+        const double uv = uniform24(seeds[b], (uint32_t)b, (uint32_t)(v - 1), 0u, round);
+        mA = std::min(mA, std::fabs(uv - ratio));
+        if (uv < ratio) {
+          u = v;
+          if (depth < Dmax) path[(int64_t)b * Dmax + depth] = v;
+          ++depth;
+          r = softmax(load_row(target, dtype, ((int64_t)b * N + v) * t_stride, V), T);
+          moved = true;
+        } else {
+          std::vector<double> w;
+          const double Z = residual(r, q, w);
+          if (Z > 1e-300) {
+            for (auto& e : w) e /= Z;
+            r = std::move(w);
+          }
+          Zlast = Z;
+        }
+      }
+      if (!moved) break;
+    }
+    double total = 0.0;
+    for (double e : r) total += e;
+    double mC = 0.0;
+    const double ub = uniform24(seeds[b], (uint32_t)b, (uint32_t)u, 1u, round);
+    bonus[b] = inverse_cdf(r, total, ub, &mC);
+    accept_len[b] = depth;
+    if (resid_mass) resid_mass[b] = Zlast < 0.0 ? total : Zlast;
+    if (margin_accept) margin_accept[b] = mA;
+    if (margin_cdf) margin_cdf[b] = mC;
+  });
+  return 0;
+}
+
+// Draft tokens of a tree: x_v ~ q_{parent(v)} by inverse CDF at
+// U(seed_b; b, v-1, 2, round) -- for a chain, the same draws as the linear
+// drafts at positions j = v-1.
+int orc_tree_draft(const void* draft, int dtype, int64_t d_stride, int B, int N, int V, double T,
+                   const int32_t* parent, const uint64_t* seeds, uint32_t round, int32_t* tokens,
+                   int nthreads) {
+  for (int u = 1; u < N; ++u)
+    if (parent[u] < 0 || parent[u] >= u) return 3;
+  parallel_rows(B, nthreads, [&](int b) {
+    tokens[(int64_t)b * N] = -1;
+    for (int v = 1; v < N; ++v) {
+      auto q = softmax(load_row(draft, dtype, ((int64_t)b * N + parent[v]) * d_stride, V), T);
+      double Z = 0.0;
+      for (double e : q) Z += e;
+      const double uv = uniform24(seeds[b], (uint32_t)b, (uint32_t)(v - 1), 2u, round);
+      tokens[(int64_t)b * N + v] = inverse_cdf(q, Z, uv, nullptr);
     }
   });
   return 0;

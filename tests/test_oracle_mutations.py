@@ -11,6 +11,7 @@ import os
 import pytest
 
 import tests.test_oracle_pins as P
+import tests.test_oracle_tree as PT
 
 MUTATIONS = {
     "residual sign flipped": ("std::max(0.0, p[y] - q[y])", "std::max(0.0, q[y] - p[y])"),
@@ -30,6 +31,13 @@ MUTATIONS = {
                                          "const double Tb = T;"),
     "greedy bonus from the runner-up": ("bonus[b] = top_n(zk, 1)[0];",
                                         "bonus[b] = top_n(zk, 2)[1];"),
+    "tree residual not renormalised": ("for (auto& e : w) e /= Z;", ""),
+    "tree accept uniform of the wrong node": ("(uint32_t)(v - 1), 0u, round)",
+                                              "(uint32_t)v, 0u, round)"),
+    "tree draft from the child's own row": ("((int64_t)b * N + parent[v]) * d_stride",
+                                            "((int64_t)b * N + v) * d_stride"),
+    "tree bonus before the last child": ("for (int v = u + 1; v < N && !moved; ++v) {",
+                                         "for (int v = u + 1; v < N - 1 && !moved; ++v) {"),
 }
 
 PINS = [
@@ -45,6 +53,9 @@ PINS = [
     lambda orc: P.test_accept_length_law_per_position_C(orc, (0.3, 0.5, 0.8, 1.0)),
     P.test_greedy_is_the_low_temperature_limit,
     P.test_per_sequence_temperature_equals_separate_calls,
+    PT.test_chain_tree_is_linear_verification,
+    lambda orc: PT.test_tree_walk_laws_monte_carlo(orc, "two-by-two"),
+    PT.test_tree_draft_follows_parent_distribution,
 ]
 
 
