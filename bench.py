@@ -170,6 +170,73 @@ def bt_rows(bb, w):
     return rows.view(np.int16) if w.dtype == "bf16" else rows
 
 
+def side_workload(name, steps, warmup, rank, dev, tdist):
+    """A second workload measured in the same process, after the headline
+    one: its verify_round launches timed one by one with CUDA events (inputs
+    resident, larger than L2), with their own roofline."""
+    import torch
+
+    import sampling_ssd_verify_gb300 as ssd
+    from ssd_inputs import WORKLOADS, make_batch
+
+    w = WORKLOADS[name]
+    B, K, Kq, V = w.B, w.K, w.Kq, w.V
+    F = np.asarray(w.fanout, dtype=np.int32)
+    bt = make_batch(w, seed=rank_seed(w, rank))
+    if w.dtype == "bf16":
+        tg = torch.from_numpy(bt["target"].view(np.int16)).to(dev).view(torch.bfloat16)
+        dg = torch.from_numpy(bt["draft"].view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        tg = torch.from_numpy(bt["target"]).to(dev)
+        dg = torch.from_numpy(bt["draft"]).to(dev)
+    seeds = torch.from_numpy(bt["seeds"].view(np.int64)).to(dev)
+    tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    for j in range(K):
+        tok[:, j] = ssd.saguaro_sample(dg[:, j, :], w.T, w.C, int(F[j]), seeds, j, 0,
+                                       guesses=False, qprime=False)["token"]
+    tok = tok.contiguous()
+    ws = torch.empty(ssd.lib().ssd_verify_workspace_size(B, K, Kq, V), dtype=torch.uint8,
+                     device=dev)
+    table = torch.empty(ssd.cache_bytes(B * Kq * int(F.max())), dtype=torch.uint8, device=dev)
+    out = {}
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s in range(warmup):
+        ssd.verify_round(tg, dg, tok, seeds, 1 + s, F, w.C, w.T, table=table, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    if tdist.is_available() and tdist.is_initialized():
+        tdist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        evs[s][0].record(stream)
+        ssd.verify_round(tg, dg, tok, seeds, 1000 + s, F, w.C, w.T, table=table, workspace=ws,
+                         out=out)
+        evs[s][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), tdist, dev)
+    launch = [a.elapsed_time(b) for a, b in evs]
+    alg = w.algorithmic_bytes()
+    hbm_peak, peak_kind = peaks()
+    achieved = alg / (float(np.mean(launch)) * 1e-3) / 1e9
+    world = tdist.get_world_size() if tdist.is_available() and tdist.is_initialized() else 1
+    return {"workload": w.name, "B": B, "K": K, "Kq": Kq, "V": V, "dtype": w.dtype, "T": w.T,
+            "C": w.C, "fanout": list(map(int, F)), "steps": steps, "warmup": warmup,
+            "value": job_rows_per_s(B * steps, world, ms * 1e-3), "unit": "rows/s",
+            "ms_per_step": ms / steps,
+            "accept_mean": float(out["accept_len"].float().mean().item()),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic_from_profile(name),
+                         "kernel": "ssd_verify_round (streaming pass, bonus draws, outcome cache)",
+                         "algorithmic_bytes_per_launch": alg,
+                         "launch_ms": float(np.mean(launch)),
+                         "launch_ms_median": float(np.median(launch)), "peak_kind": peak_kind},
+            "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else "inputs smaller than L2"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as tdist
@@ -354,6 +421,11 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ne}
 
+    # the batched bf16 workload, measured in the same process with its own roofline
+    side = None
+    if args.side and args.side != args.workload and not (args.batch or args.vocab):
+        side = side_workload(args.side, args.steps, args.warmup, rank, dev, tdist)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -393,6 +465,7 @@ def run_ours(args):
                          "tail_bytes_per_launch": tail_bytes,
                          "peak_kind": peak_kind},
             "e2e": e2e,
+            "workloads": {args.side: side} if side else None,
             "gpu_launches": args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
@@ -501,6 +574,8 @@ def main():
     ap.add_argument("--workload", default="c5", choices=["c2", "c3", "c4", "c5"])
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch B")
     ap.add_argument("--vocab", type=int, default=0, help="override the workload's vocabulary V")
+    ap.add_argument("--side", default="c3", help="second workload measured in the same run "
+                    "(empty: none)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -69,6 +69,7 @@ typedef enum {
 #define SSD_DEV_DUPLICATE_KEY 0x10 /* cache insert met an existing key */
 #define SSD_DEV_BAD_TEMPERATURE 0x20 /* a per-sequence temperature negative or not
                                         finite; that sequence is verified greedily */
+#define SSD_DEV_BAD_FANOUT 0x40    /* a per-row fan-out outside [0, Fmax]; clamped */
 
 typedef enum { SSD_BF16 = 0, SSD_F32 = 1 } ssd_dtype;
 
@@ -235,7 +236,9 @@ ssd_status ssd_verify_round(const ssd_logits* target, const ssd_logits* draft, i
  *     B = 256 sequences with K = 8 at V = 151936.
  *   - The first call on a device looks up the array's address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture on the device.
+ *     that first call before any stream capture on the device.  The cache is
+ *     keyed on the current context: after cudaDeviceReset the next call
+ *     looks the address up again (make it, too, outside stream capture).
  *   - All calls on a device share the array; the parts that must start at
  *     zero are cleared at the start of each call.  Calls whose work overlaps
  *     on the GPU (different streams or host threads) race on the array and
@@ -272,9 +275,11 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
 /* ---------------------------------------------------------------------------
  * ssd_saguaro_sample -- one continuation step of the SSD cache build: every
  * branch row draws its next draft token from the Saguaro distribution.
- * [SSD-note] §"Saguaro 优化二：Saguaro 采样" and §"实现细节：缓存怎么建".
+ * [SSD-note] §"Saguaro 优化二：Saguaro 采样" and §"实现细节：缓存怎么建"; the
+ * fan-out of a branch row is that of the outcome position it continues
+ * (§"最优扇出度分配"), so it is given per row.
  *
- * For branch row r (0 <= r < R):
+ * For branch row r (0 <= r < R) with F = F_row[r]:
  *   S = top-F of z[r,:];  q' = Saguaro(softmax(z[r,:]/T), S, C);
  *   x = smallest y with sum_{y'<=y} q'(y') > u * sum(q'),
  *       u = U(seeds[r]; r, j, 2, round);
@@ -284,17 +289,65 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
  * T           temperature, finite and > 0.
  * C           Saguaro factor in (0, 1] (the factor of position j when the
  *             caller uses one per position).
- * F           cached-set size / guesses per row, 0..SSD_MAX_F.
+ * F_row       device [R] int32 cached-set size / guesses per row, each in
+ *             [0, Fmax] (a value outside is clamped and sets
+ *             SSD_DEV_BAD_FANOUT), or NULL: F = Fmax for every row.
+ * Fmax        0..SSD_MAX_F, Fmax + 1 <= V: the largest F and the column
+ *             count of out_guess.
  * seeds       device [R] uint64.   j: continuation position (counter word).
  * out_token   device [R] int32 out.
  * out_qprime  device [R] float out (or NULL): q'(x).
- * out_guess   device [R, F] int32 out (or NULL).
+ * out_guess   device [R, Fmax] int32 out (or NULL), -1 padded.
  * ------------------------------------------------------------------------- */
 size_t ssd_saguaro_workspace_size(int R, int V);
-ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, float C, int F,
-                              const uint64_t* seeds, int j, uint32_t round, int32_t* out_token,
-                              float* out_qprime, int32_t* out_guess, void* workspace,
-                              size_t workspace_bytes, int32_t* dev_status, void* stream);
+ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, float C,
+                              const int32_t* F_row, int Fmax, const uint64_t* seeds, int j,
+                              uint32_t round, int32_t* out_token, float* out_qprime,
+                              int32_t* out_guess, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ssd_tree_verify -- verification of tree-shaped drafts.  [SD-7.3] §7.3.9
+ * item 3 (树形草稿: several candidate continuations per position instead of
+ * one chain); the pages give no algorithm, and the per-token rule of §7.3.3
+ * is applied to each candidate in turn (multi-candidate rejection sampling):
+ *
+ * The tree has N nodes, the same for the whole batch: node 0 is the last
+ * verified position, node u >= 1 has parent parent[u] < u and holds draft
+ * token tokens[b, u], drawn from the draft distribution q_{parent(u)} of its
+ * parent.  Target row u of tree b is p_u, the target distribution after node
+ * u's path; draft row u is q_u.  For tree b:
+ *   u = 0, r = p_0 = softmax(z_target[b,0,:] / T);
+ *   for each child v of u in increasing index order:
+ *     accept x_v iff U(seeds[b]; b, v-1, 0, round) < r(x_v) / q_u(x_v):
+ *       then u = v, r = p_v, and continue with v's children;
+ *     else r = (r - q_u)^+ / sum (r - q_u)^+;
+ *   when no child of u is accepted (or u is a leaf): bonus t = smallest y
+ *   with sum_{y'<=y} r(y') > U(seeds[b]; b, u, 1, round) * sum(r).
+ * A chain (parent[u] = u - 1) gives ssd_verify's results with C = 1, F = 0
+ * (accept_len, bonus; drafts drawn with counter (b, v-1, 2, round)).
+ *
+ * target, draft  [B, N, V] logits, same dtype: row (b, u) is row b*N + u.
+ * parent      HOST [N] int32: parent[0] = -1, 0 <= parent[u] < u.
+ * tokens      device [B, N] int32 (entry 0 of a tree is ignored).
+ * accept_len  device [B] int32 out: depth of the last accepted node.
+ * path        device [B, Dmax] int32 out (or NULL): the accepted nodes, -1
+ *             padded; Dmax >= the tree's depth.
+ * bonus       device [B] int32 out.
+ * resid_mass  device [B] float out (or NULL): sum (r - q_u)^+ of the last
+ *             rejection at the final node, 1 when it rejected nothing.
+ * T           temperature, finite and > 0.   N <= 256.
+ * workspace   >= ssd_tree_workspace_size(B, N, V), 256-byte aligned.
+ * Two launches on `stream`: the streaming pass normalises every row, then
+ * one CTA per tree walks it.
+ * ------------------------------------------------------------------------- */
+size_t ssd_tree_workspace_size(int B, int N, int V);
+ssd_status ssd_tree_verify(const ssd_logits* target, const ssd_logits* draft, int B, int N, int V,
+                           float T, const int32_t* parent, const int32_t* tokens,
+                           const uint64_t* seeds, uint32_t round, int32_t* accept_len,
+                           int32_t* path, int Dmax, int32_t* bonus, float* resid_mass,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream);
 
 /* ---------------------------------------------------------------------------
  * Outcome cache.  [SSD-note] §"SSD 的核心思想": the verification outcome is the

@@ -27,10 +27,10 @@ from . import _build
 
 __all__ = [
     "SSDError", "build", "lib", "verify", "verify_round", "verify_host", "topf_bonus",
-    "saguaro_sample",
+    "saguaro_sample", "tree_verify",
     "cache_bytes", "cache_build", "cache_build_guesses", "cache_lookup", "fanout",
     "DEV_BAD_TOKEN", "DEV_ZERO_RESIDUAL", "DEV_TIMEOUT", "DEV_TABLE_FULL", "DEV_DUPLICATE_KEY",
-    "DEV_BAD_TEMPERATURE",
+    "DEV_BAD_TEMPERATURE", "DEV_BAD_FANOUT",
 ]
 
 DEV_BAD_TOKEN = 0x1
@@ -39,6 +39,7 @@ DEV_TIMEOUT = 0x4
 DEV_TABLE_FULL = 0x8
 DEV_DUPLICATE_KEY = 0x10
 DEV_BAD_TEMPERATURE = 0x20
+DEV_BAD_FANOUT = 0x40
 
 SSD_BF16, SSD_F32 = 0, 1
 _lib = None
@@ -75,8 +76,11 @@ _SIGS = {
     "ssd_topf_bonus": ([_LP, _i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, _vp, _vp, _vp, _sz,
                         _vp, _vp], _i),
     "ssd_saguaro_workspace_size": ([_i, _i], _sz),
-    "ssd_saguaro_sample": ([_LP, _i, _i, ctypes.c_float, ctypes.c_float, _i, _vp, _i,
+    "ssd_saguaro_sample": ([_LP, _i, _i, ctypes.c_float, ctypes.c_float, _vp, _i, _vp, _i,
                             ctypes.c_uint32, _vp, _vp, _vp, _vp, _sz, _vp, _vp], _i),
+    "ssd_tree_workspace_size": ([_i, _i, _i], _sz),
+    "ssd_tree_verify": ([_LP, _LP, _i, _i, _i, ctypes.c_float, _vp, _vp, _vp, ctypes.c_uint32,
+                         _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp, _vp], _i),
     "ssd_cache_bytes": ([_i], _sz),
     "ssd_cache_build": ([_vp, _sz, _vp, _vp, _vp, _vp, _i, _vp, _vp], _i),
     "ssd_cache_build_guesses": ([_vp, _sz, _vp, _i, _i, _i, _vp, _vp], _i),
@@ -348,28 +352,87 @@ def topf_bonus(draft, fanout, T=1.0, draft_tokens=None, K=None, Fmax=None, guess
 
 
 def saguaro_sample(rows, T, C, F, seeds, j, round_, guesses=True, qprime=True, workspace=None,
-                   dev_status=None, stream=None, out=None):
-    """ssd_saguaro_sample over branch rows [R, V]: token, qprime, guesses."""
+                   dev_status=None, stream=None, out=None, Fmax=None):
+    """ssd_saguaro_sample over branch rows [R, V]: token, qprime, guesses.
+
+    F: one fan-out for every row (an int), or one per row -- a device int32
+    tensor [R] (then Fmax, the largest, must be given) or anything numpy
+    reads (uploaded here).  guesses are [R, Fmax], -1 padded."""
     torch = _torch()
     R, V = rows.shape[-2], rows.shape[-1]
     dev = rows.device
+    F_row = None
+    if np.ndim(F) == 0 and not hasattr(F, "is_cuda"):
+        Fm = int(F)
+    elif hasattr(F, "is_cuda"):
+        if Fmax is None:
+            raise SSDError("a device F tensor needs Fmax")
+        F_row, Fm = _i32(F), int(Fmax)
+    else:
+        Fa = np.ascontiguousarray(F, dtype=np.int32)
+        if Fa.shape != (R,):
+            raise SSDError("per-row F must have R entries")
+        Fm = int(Fa.max()) if Fmax is None else int(Fmax)
+        F_row = torch.from_numpy(Fa).to(dev)
+    if F_row is not None and F_row.shape != (R,):
+        raise SSDError("per-row F must have R entries")
     o = out if out is not None else {}
     if "token" not in o:
         o["token"] = torch.empty(R, dtype=torch.int32, device=dev)
         if qprime:
             o["qprime"] = torch.empty(R, dtype=torch.float32, device=dev)
-        if guesses and F > 0:
-            o["guesses"] = torch.empty((R, F), dtype=torch.int32, device=dev)
+        if guesses and Fm > 0:
+            o["guesses"] = torch.empty((R, Fm), dtype=torch.int32, device=dev)
     L = lib()
     ws = workspace if workspace is not None else _workspace(L.ssd_saguaro_workspace_size(R, V),
                                                             dev)
     rl = _logits(rows)
-    st = L.ssd_saguaro_sample(ctypes.byref(rl), R, V, float(T), float(C), int(F),
+    st = L.ssd_saguaro_sample(ctypes.byref(rl), R, V, float(T), float(C), _dev_ptr(F_row), Fm,
                               _dev_ptr(_u64_seeds(seeds, dev)), int(j),
                               int(round_) & 0xFFFFFFFF, _dev_ptr(o["token"]),
                               _dev_ptr(o.get("qprime")), _dev_ptr(o.get("guesses")),
                               _dev_ptr(ws), ws.numel(), _dev_ptr(dev_status), _stream(stream))
     _check(st, "ssd_saguaro_sample")
+    return o
+
+
+def tree_verify(target, draft, parent, tokens, seeds, round_, T=1.0, workspace=None,
+                dev_status=None, stream=None, out=None):
+    """ssd_tree_verify: target, draft [B, N, V] (row u of a tree: p_u / q_u at
+    node u), parent: N ints (parent[0] = -1, parent[u] < u), tokens int32
+    [B, N] on the device.  Returns accept_len [B], path [B, depth], bonus
+    [B] and resid_mass [B] (device tensors)."""
+    torch = _torch()
+    B, N, V = target.shape
+    dev = target.device
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    if par.shape != (N,):
+        raise SSDError("parent must have N entries")
+    depth = np.zeros(N, dtype=np.int64)
+    for u in range(1, N):
+        if not 0 <= par[u] < u:
+            raise SSDError("parent[u] must lie in [0, u)")
+        depth[u] = depth[par[u]] + 1
+    Dmax = max(1, int(depth.max()))
+    o = out if out is not None else {}
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["path"] = torch.empty((B, Dmax), dtype=torch.int32, device=dev)
+        o["bonus"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["resid_mass"] = torch.empty(B, dtype=torch.float32, device=dev)
+    L = lib()
+    wsb = L.ssd_tree_workspace_size(B, N, V)
+    if wsb == 0:
+        raise SSDError("invalid tree shape")
+    ws = workspace if workspace is not None else _workspace(wsb, dev)
+    tl, dl = _logits(target), _logits(draft)
+    st = L.ssd_tree_verify(ctypes.byref(tl), ctypes.byref(dl), B, N, V, float(T),
+                           par.ctypes.data_as(ctypes.c_void_p), _dev_ptr(_i32(tokens)),
+                           _dev_ptr(_u64_seeds(seeds, dev)), int(round_) & 0xFFFFFFFF,
+                           _dev_ptr(o["accept_len"]), _dev_ptr(o["path"]), Dmax,
+                           _dev_ptr(o["bonus"]), _dev_ptr(o["resid_mass"]), _dev_ptr(ws),
+                           ws.numel(), _dev_ptr(dev_status), _stream(stream))
+    _check(st, "ssd_tree_verify")
     return o
 
 

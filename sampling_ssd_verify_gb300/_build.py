@@ -19,7 +19,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libssd.so")
 CHECKS_LIB_PATH = os.path.join(PKG, "libssd_checks.so")
-SOURCES = ["ssd_stream.cu", "ssd_cache.cu", "ssd_api.cu", "ssd_noalloc.cu"]
+SOURCES = ["ssd_stream_bf16.cu", "ssd_stream_f32.cu", "ssd_cache.cu", "ssd_api.cu",
+           "ssd_noalloc.cu", "ssd_tree.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

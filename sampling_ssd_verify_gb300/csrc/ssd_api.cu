@@ -40,72 +40,104 @@ bool logits_ok(const ssd_logits* L, int V) {
 
 bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
 
-int topk_for(int maxF) {
-  const int need = maxF + 1;
-  if (need <= 2) return 2;
-  if (need <= 4) return 4;
-  if (need <= 8) return 8;
-  return 16;
-}
-
 ssd_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return SSD_OK;
   cudaGetLastError();  // clear a sticky launch-configuration error
   return SSD_ERR_CUDA;
 }
 
-// Chunks per row of the streaming pass.  CTAs take chunks from a global
-// counter, so a CTA that meets costlier rows (more top-list insertions)
-// takes fewer.  Whole rows when there are at least two per CTA (a row split
-// over CTAs costs a partial merge and restarts its top-list pruning);
-// otherwise rows are cut into up to kMaxChunks equal non-empty chunks: about
-// four per CTA in all, or, for a few rows (a latency-bound pass), at most
-// one per CTA.  The launch and the workspace size both use it.
 int64_t stream_grid0() {
   int sms = num_sms();
   if (sms <= 0) sms = 1;
   return std::min<int64_t>(sms, kMaxGrid);
 }
 
-int stream_chunk_len(int64_t NR, int upr) {
-  const int64_t grid0 = stream_grid0();
-  int64_t nch = 1;
-  if (2 * NR <= grid0) {
-    // a few rows (small batches): latency-bound, so one round of chunks
-    nch = grid0 / NR;
-  } else if (NR < 2 * grid0) {
-    nch = (4 * grid0 + NR - 1) / NR;
-  }
-  nch = std::max<int64_t>(1, std::min<int64_t>({nch, (int64_t)kMaxChunks, (int64_t)upr}));
-  return (int)((upr + nch - 1) / nch);
-}
-
-int stream_chunks_per_row(int64_t NR, int upr) {
-  const int clen = stream_chunk_len(NR, upr);
-  return (upr + clen - 1) / clen;
-}
-
 int units_per_row(int V) { return (V + kUnitA - 1) / kUnitA; }
+
+// Chunking of the streaming pass: nch chunks of clen units per row.  CTAs
+// take chunks from a global counter, so a CTA that meets costlier rows takes
+// fewer.  Whole rows when there are at least two per CTA (a row split over
+// CTAs costs a partial merge); otherwise rows are cut into chunks of whole
+// stages: about four per CTA in all, or, for a few rows (a latency-bound
+// pass), at most one per CTA.  A chunk has at most kMaxChunkStages stages
+// (its block maxima live in shared memory).  The launch and the workspace
+// size both use it.
+void stream_chunking(int64_t NR, int V, int esize, int& nch, int& clen) {
+  const int64_t grid0 = stream_grid0();
+  const int ups = units_per_stage(esize);
+  const int upr = units_per_row(V);
+  const int spr = (upr + ups - 1) / ups;
+  int64_t want = 1;
+  if (2 * NR <= grid0) {
+    want = grid0 / NR;
+  } else if (NR < 2 * grid0) {
+    want = (4 * grid0 + NR - 1) / NR;
+  }
+  want = std::max<int64_t>(want, (spr + kMaxChunkStages - 1) / kMaxChunkStages);
+  want = std::max<int64_t>(1, std::min<int64_t>(want, spr));
+  const int sper = (int)((spr + want - 1) / want);  // stages per chunk
+  clen = sper * ups;
+  nch = (upr + clen - 1) / clen;
+  if (nch == 1) clen = upr;
+}
+
+// Chunks per group of the draws: enough for about one per CTA when groups
+// are few, each at least one stage.
+int draw_chunks_per_group(int groups, int V, int esize) {
+  const int64_t grid0 = stream_grid0();
+  const int nsub = (V + kUnitB - 1) / kUnitB;
+  const int ups = fused_units_per_stage(esize);
+  const int stages = (nsub + ups - 1) / ups;
+  int64_t cpg = (grid0 + groups - 1) / groups;
+  cpg = std::max<int64_t>(1, std::min<int64_t>(cpg, stages));
+  const int cu = (int)((nsub + cpg - 1) / cpg);
+  return (nsub + cu - 1) / cu;
+}
+
+WsLayout layout_for(int groups, int rpg, int K, int V, int esize, bool draws, bool bsum) {
+  int nch, clen;
+  stream_chunking((int64_t)groups * rpg, V, esize, nch, clen);
+  const int cpg = draws ? draw_chunks_per_group(groups, V, esize) : 0;
+  return ws_layout(groups, rpg, K, V, esize, nch, cpg, bsum);
+}
+
+// Workspace bytes for either element type.
+size_t layout_bytes(int groups, int rpg, int K, int V, bool draws, bool bsum) {
+  return std::max(layout_for(groups, rpg, K, V, 2, draws, bsum).total,
+                  layout_for(groups, rpg, K, V, 4, draws, bsum).total);
+}
+
+// The 16-byte-aligned rows of whole vectors whose one-term draws can use the
+// streaming pass's block sums.
+bool rows_aligned(const ssd_logits* L, int V) {
+  const int es = esize_of(L->dtype);
+  return ((uintptr_t)L->ptr % 16) == 0 && (L->row_stride * es) % 16 == 0 && (V * es) % 16 == 0;
+}
 
 struct Common {
   StreamParams sp;
   CdfParams cp;
 };
 
-// Shared set-up of the streaming pass and the CDF pass over `groups` groups of
-// rpg = nt + nd rows.
+// Shared set-up of a launch over `groups` groups of rpg = nt + nd rows: the
+// workspace layout, its counters cleared on the stream, the parameter
+// blocks of the streaming pass and of the draws.
 ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, int K, int Kq,
                  int nt, int nd, int V, float T, void* workspace, size_t ws_bytes,
-                 cudaStream_t stream, Common& cm, WsLayout& L, bool usum = false) {
+                 cudaStream_t stream, Common& cm, bool draws, bool bsum) {
   const int rpg = nt + nd;
-  L = ws_layout(groups, rpg, V,
-                stream_chunks_per_row((int64_t)groups * rpg, units_per_row(V)), usum);
+  const int es = esize_of(draft->dtype);
+  int nch, clen;
+  stream_chunking((int64_t)groups * rpg, V, es, nch, clen);
+  const int cpg = draws ? draw_chunks_per_group(groups, V, es) : 0;
+  const WsLayout L = ws_layout(groups, rpg, K, V, es, nch, cpg, bsum);
   if (workspace == nullptr || ((uintptr_t)workspace & 255) != 0 || ws_bytes < L.total)
     return SSD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   cudaError_t e = cudaMemsetAsync(ws + L.cnt_off, 0, L.cnt_bytes, stream);
   if (e != cudaSuccess) return cuda_status(e);
   int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
+  unsigned long long* w8 = reinterpret_cast<unsigned long long*>(ws + L.cnt_off + L.ctr_off);
   StreamParams& p = cm.sp;
   p = StreamParams{};
   p.tgt = target ? target->ptr : nullptr;
@@ -121,22 +153,26 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.rpg = rpg;
   p.NR = L.NR;
   p.upr = units_per_row(V);
-  p.total_units = L.NR * p.upr;
+  p.spr = L.nblk / kConsumerWarps;
+  p.nblk = L.nblk;
+  p.nch = nch;
+  p.clen = clen;
+  p.nchunks = L.NR * nch;
+  p.order = 0;
   p.c = (float)(1.4426950408889634 / (double)T);  // log2(e) / T
-  p.row_cnt = cnt;
-  p.grp_cnt = cnt + L.NR;
-  p.row_cut = reinterpret_cast<uint32_t*>(cnt + L.NR + 2 * groups);
-  p.grp_ready = cnt + 2 * L.NR + 2 * groups;
-  p.chunk_ctr = reinterpret_cast<unsigned long long*>(ws + L.cnt_off + L.ctr_off);
+  p.row_cnt = cnt + L.o_row_cnt;
+  p.pair_cnt = cnt + L.o_pair;
+  p.kcnt = cnt + L.o_kcnt;
+  p.dq_entry = cnt + L.o_dq;
+  p.seq_state = reinterpret_cast<unsigned long long*>(ws + L.cnt_off) + L.o_state;
+  p.chunk_ctr = w8;
+  p.dq_tail = reinterpret_cast<unsigned int*>(w8 + 3);
+  p.dq_head = reinterpret_cast<unsigned int*>(w8 + 4);
+  p.decided = reinterpret_cast<int*>(w8 + 5);
   p.partials = reinterpret_cast<RowPartial*>(ws + L.part_off);
   p.rowres = reinterpret_cast<RowResult*>(ws + L.rowres_off);
   p.gparams = reinterpret_cast<GroupParams*>(ws + L.gp_off);
-  if (usum) {
-    p.usum = reinterpret_cast<float2*>(ws + L.usum_off);
-    const int su = 32 * (16 / esize_of(draft->dtype));  // 32 vectors of 16 bytes
-    p.nsu = (V + su - 1) / su;
-  }
-  const int es = esize_of(draft->dtype);
+  p.bsum = bsum ? reinterpret_cast<float2*>(ws + L.bsum_off) : nullptr;
   if (target != nullptr) {
     p.t_lo = static_cast<const char*>(target->ptr);
     p.t_hi = p.t_lo + ((int64_t)(groups * (K + 1) - 1) * target->row_stride + V) * es;
@@ -158,12 +194,15 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   q.V = V;
   q.nsub = L.nsub;
   q.total_units = (int64_t)groups * L.nsub;
+  q.cpg = cpg;
+  q.cu = cpg > 0 ? (L.nsub + cpg - 1) / cpg : 0;
+  q.nchunks = (int64_t)groups * cpg;
   q.gp = p.gparams;
   q.rowres = p.rowres;
   q.rpg = rpg;
   q.nt = nt;
   q.subsum = reinterpret_cast<float*>(ws + L.sub_off);
-  q.cnt = cnt + L.NR + groups;
+  q.cnt = cnt + L.o_grp_cnt;
   q.t_lo = p.t_lo;
   q.t_hi = p.t_hi;
   q.d_lo = p.d_lo;
@@ -172,38 +211,16 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   return SSD_OK;
 }
 
-// Chunking of the streaming pass and, when `draws`, of the draws that follow
-// it in the same launch; then the launch.
-//
-// Draws: units of kUnitB elements, fused_units_per_stage per ring stage, cut
-// into chunks of cu units -- about four per CTA in all, at most eight stages
-// each (a small pass, latency-bound, takes one round) -- and taken group by
-// group, the order in which the streaming pass completes the groups, so
-// that a chunk rarely waits for its group's parameters.
-ssd_status run_pass(Common& cm, int dtype, int topk, bool draws, cudaStream_t s) {
-  StreamParams& p = cm.sp;
-  CdfParams& q = cm.cp;
-  const int64_t grid0 = stream_grid0();
-  p.clen = stream_chunk_len(p.NR, p.upr);
-  p.nch = (p.upr + p.clen - 1) / p.clen;
-  p.nchunks = p.NR * p.nch;
-  q.nchunks = 0;
-  if (draws) {
-    const int ups = fused_units_per_stage(esize_of(dtype));
-    int64_t cu = q.total_units >= 8 * grid0 ? (q.total_units + 4 * grid0 - 1) / (4 * grid0)
-                                            : (q.total_units + grid0 - 1) / grid0;
-    cu = std::max<int64_t>(1, std::min<int64_t>({cu, 8 * (int64_t)ups, (int64_t)q.nsub}));
-    q.cu = (int)cu;
-    q.cpg = (q.nsub + q.cu - 1) / q.cu;
-    q.nchunks = (int64_t)q.groups * q.cpg;
-  } else {
-    p.grp_ready = nullptr;
-  }
+// The launch: one CTA per SM, at most one per chunk of work.
+ssd_status run_pass(Common& cm, int dtype, cudaStream_t s) {
   VerifyParams vp;
-  vp.s = p;
-  vp.q = q;
-  const int grid = (int)std::min<int64_t>(grid0, p.nchunks + q.nchunks);
-  return cuda_status(launch_stream(vp, dtype, topk, grid, s));
+  vp.s = cm.sp;
+  vp.q = cm.cp;
+  const int grid =
+      (int)std::max<int64_t>(1, std::min<int64_t>(stream_grid0(), vp.s.nchunks + vp.q.nchunks));
+  const cudaError_t e = dtype == SSD_BF16 ? launch_stream_dt<0>(vp, grid, s)
+                                          : launch_stream_dt<1>(vp, grid, s);
+  return cuda_status(e);
 }
 
 int64_t capacity_of(size_t table_bytes) {
@@ -260,18 +277,17 @@ ssd_status ssd_fanout(int K, int budget, double a, double r, int32_t* F_out) {
 size_t ssd_verify_workspace_size(int B, int K, int Kq, int V) {
   if (B < 1 || K < 1 || K > SSD_MAX_K || (Kq != K && Kq != K + 1) || V < 2 || V > SSD_MAX_V)
     return 0;
-  return ws_layout(B, K + 1 + Kq, V,
-                   stream_chunks_per_row((int64_t)B * (K + 1 + Kq), units_per_row(V))).total;
+  return layout_bytes(B, K + 1 + Kq, K, V, true, true);
 }
 
 size_t ssd_topf_workspace_size(int B, int Kq, int V) {
   if (B < 1 || Kq < 1 || Kq > SSD_MAX_K + 1 || V < 2 || V > SSD_MAX_V) return 0;
-  return ws_layout(B, Kq, V, stream_chunks_per_row((int64_t)B * Kq, units_per_row(V))).total;
+  return layout_bytes(B, Kq, 0, V, false, false);
 }
 
 size_t ssd_saguaro_workspace_size(int R, int V) {
   if (R < 1 || V < 2 || V > SSD_MAX_V) return 0;
-  return ws_layout(R, 1, V, stream_chunks_per_row((int64_t)R, units_per_row(V)), true).total;
+  return layout_bytes(R, 1, 0, V, true, true);
 }
 
 }  // extern "C"
@@ -330,28 +346,31 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
   const bool need_top = (guesses && maxF > 0) || biased;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Common cm;
-  WsLayout L;
   // a greedy sequence's (unused) sums take T = 1
   const bool greedy_all = T_rows == nullptr && T == 0.f;
+  // all-accepted bonus draws of p_K from the streaming pass's block sums
+  const bool direct = rows_aligned(target, V);
   ssd_status st = setup(target, draft, B, K, Kq, K + 1, Kq, V, T > 0.f ? T : 1.f, workspace,
-                        workspace_bytes, s, cm, L);
+                        workspace_bytes, s, cm, true, direct);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
   for (int j = 0; j <= SSD_MAX_K; ++j) {
     p.F[j] = F[j];
     p.C[j] = j < K ? Cv[j] : 1.f;
   }
+  p.order = 1;  // position-major: outcomes are decided while later positions stream
   p.T_rows = T_rows;
   p.greedy_all = greedy_all ? 1 : 0;
   p.bonus = bonus;
   p.resid_mass = resid_mass;
   if (ra != nullptr) {
+    unsigned long long* w8 = p.chunk_ctr;
     p.rc.table = ra->table;
     p.rc.cap = cache_cap;
     p.rc.branch = ra->out_branch;
     p.rc.all_hit = ra->all_hit;
-    p.rc.cnt = p.chunk_ctr + 1;
-    p.rc.cleared = reinterpret_cast<int*>(p.chunk_ctr + 2);
+    p.rc.cnt = w8 + 1;
+    p.rc.cleared = reinterpret_cast<int*>(w8 + 2);
     cm.cp.rc = p.rc;
   }
   p.need_top = need_top ? 1 : 0;
@@ -370,10 +389,7 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
   q.out_token = bonus;
   q.out_mass = resid_mass;
   q.status = dev_status;
-  // greedy sequences keep a one-entry list (the argmax) on their target rows
-  int topk = need_top ? topk_for(maxF) : 0;
-  if (T_rows != nullptr || greedy_all) topk = std::max(topk, 2);
-  return run_pass(cm, target->dtype, topk, true, s);
+  return run_pass(cm, target->dtype, s);
 }
 
 }  // namespace
@@ -458,8 +474,8 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
   if (Fmax < 1 || Fmax < maxF) return SSD_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Common cm;
-  WsLayout L;
-  ssd_status st = setup(nullptr, draft, B, 0, Kq, 0, Kq, V, T, workspace, workspace_bytes, s, cm, L);
+  ssd_status st = setup(nullptr, draft, B, 0, Kq, 0, Kq, V, T, workspace, workspace_bytes, s, cm,
+                        false, false);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
   for (int j = 0; j <= SSD_MAX_K; ++j) {
@@ -474,34 +490,33 @@ ssd_status ssd_topf_bonus(const ssd_logits* draft, int B, int Kq, int V, float T
   p.guess_q = guess_q;
   p.Fmax = Fmax;
   p.status = dev_status;
-  return run_pass(cm, draft->dtype, maxF > 0 ? topk_for(maxF) : 0, false, s);
+  return run_pass(cm, draft->dtype, s);
 }
 
-ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, float C, int F,
-                              const uint64_t* seeds, int j, uint32_t round, int32_t* out_token,
-                              float* out_qprime, int32_t* out_guess, void* workspace,
-                              size_t workspace_bytes, int32_t* dev_status, void* stream) {
+ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, float C,
+                              const int32_t* F_row, int Fmax, const uint64_t* seeds, int j,
+                              uint32_t round, int32_t* out_token, float* out_qprime,
+                              int32_t* out_guess, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, void* stream) {
   if (R < 1 || V < 2 || V > SSD_MAX_V || !logits_ok(draft, V)) return SSD_ERR_INVALID_ARG;
   if (!finite_pos(T) || !std::isfinite(C) || !(C > 0.f) || C > 1.f) return SSD_ERR_INVALID_ARG;
-  if (F < 0 || F + 1 > V || !seeds || !out_token || j < 0) return SSD_ERR_INVALID_ARG;
-  if (F > SSD_MAX_F) return SSD_ERR_UNSUPPORTED;
+  if (Fmax < 0 || Fmax + 1 > V || !seeds || !out_token || j < 0) return SSD_ERR_INVALID_ARG;
+  if (Fmax > SSD_MAX_F) return SSD_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Common cm;
-  WsLayout L;
   // Aligned rows of whole 16-byte vectors: the streaming pass writes the
-  // sub-unit sums the draw needs, and each row draws as soon as it is done,
+  // block sums the draw needs, and each row draws as soon as it is done,
   // without reading the row again.
-  const int es = esize_of(draft->dtype);
-  const bool direct = ((uintptr_t)draft->ptr % 16) == 0 && (draft->row_stride * es) % 16 == 0 &&
-                      (V * es) % 16 == 0;
-  ssd_status st = setup(nullptr, draft, R, 0, 1, 0, 1, V, T, workspace, workspace_bytes, s, cm, L,
-                        direct);
+  const bool direct = rows_aligned(draft, V);
+  ssd_status st = setup(nullptr, draft, R, 0, 1, 0, 1, V, T, workspace, workspace_bytes, s, cm,
+                        !direct, direct);
   if (st != SSD_OK) return st;
   StreamParams& p = cm.sp;
-  p.F[0] = F;
-  for (int j = 0; j <= SSD_MAX_K; ++j) p.C[j] = j == 0 ? C : 1.f;
-  const bool need_top = F > 0;
-  p.need_top = need_top;
+  p.F[0] = Fmax;
+  p.F_rows = F_row;
+  p.Fmax = Fmax;
+  for (int i = 0; i <= SSD_MAX_K; ++i) p.C[i] = i == 0 ? C : 1.f;
+  p.need_top = Fmax > 0;
   p.seeds = seeds;
   p.round = round;
   p.jpos = j;
@@ -511,10 +526,86 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
   q.mode = kModeSaguaro;
   q.out_token = out_token;
   q.out_qprime = out_qprime;
-  q.out_guess = F > 0 ? out_guess : nullptr;
-  q.F = F;
+  q.out_guess = Fmax > 0 ? out_guess : nullptr;
+  q.F = Fmax;
+  q.F_rows = F_row;
   q.status = dev_status;
-  return run_pass(cm, draft->dtype, need_top ? topk_for(F) : 0, !direct, s);
+  return run_pass(cm, draft->dtype, s);
+}
+
+size_t ssd_tree_workspace_size(int B, int N, int V) {
+  if (B < 1 || N < 1 || N > kMaxTreeNodes || V < 2 || V > SSD_MAX_V) return 0;
+  return layout_bytes(B, 2 * N, N - 1, V, false, false);
+}
+
+ssd_status ssd_tree_verify(const ssd_logits* target, const ssd_logits* draft, int B, int N, int V,
+                           float T, const int32_t* parent, const int32_t* tokens,
+                           const uint64_t* seeds, uint32_t round, int32_t* accept_len,
+                           int32_t* path, int Dmax, int32_t* bonus, float* resid_mass,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  if (B < 1 || N < 1 || N > kMaxTreeNodes || V < 2 || V > SSD_MAX_V) return SSD_ERR_INVALID_ARG;
+  if (!logits_ok(target, V) || !logits_ok(draft, V) || target->dtype != draft->dtype)
+    return SSD_ERR_INVALID_ARG;
+  if (!finite_pos(T) || !parent || !tokens || !seeds || !accept_len || !bonus)
+    return SSD_ERR_INVALID_ARG;
+  if (parent[0] != -1) return SSD_ERR_INVALID_ARG;
+  int depth[kMaxTreeNodes] = {0};
+  int dmax = 0;
+  for (int u = 1; u < N; ++u) {
+    if (parent[u] < 0 || parent[u] >= u) return SSD_ERR_INVALID_ARG;
+    depth[u] = depth[parent[u]] + 1;
+    dmax = std::max(dmax, depth[u]);
+  }
+  if (path && Dmax < dmax) return SSD_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Common cm;
+  // every node's target and draft row: group b holds target rows b*N .. and
+  // draft rows b*N .. (K + 1 = Kq = N)
+  ssd_status st = setup(target, draft, B, N - 1, N, N, N, V, T, workspace, workspace_bytes, s, cm,
+                        false, false);
+  if (st != SSD_OK) return st;
+  StreamParams& p = cm.sp;
+  for (int j = 0; j <= SSD_MAX_K; ++j) {
+    p.F[j] = 0;
+    p.C[j] = 1.f;
+  }
+  p.mode = kModeTopF;
+  p.status = dev_status;
+  st = run_pass(cm, target->dtype, s);
+  if (st != SSD_OK) return st;
+  TreeParams tp{};
+  tp.B = B;
+  tp.N = N;
+  tp.V = V;
+  tp.c = p.c;
+  tp.tgt = p.tgt;
+  tp.t_stride = p.t_stride;
+  tp.dft = p.dft;
+  tp.d_stride = p.d_stride;
+  tp.tokens = tokens;
+  tp.seeds = seeds;
+  tp.round = round;
+  tp.rowres = p.rowres;
+  tp.gparams = p.gparams;
+  int n = 0;
+  for (int u = 0; u < N; ++u) {
+    tp.child_off[u] = n;
+    for (int v = u + 1; v < N; ++v)
+      if (parent[v] == u) tp.child[n++] = v;
+  }
+  tp.child_off[N] = n;
+  tp.accept_len = accept_len;
+  tp.path = path;
+  tp.Dmax = Dmax;
+  tp.resid_mass = resid_mass;
+  tp.status = dev_status;
+  tp.q = cm.cp;
+  tp.q.mode = kModeVerify;
+  tp.q.out_token = bonus;
+  tp.q.status = dev_status;
+  const cudaError_t e = target->dtype == SSD_BF16 ? launch_tree_dt<0>(tp, s) : launch_tree_dt<1>(tp, s);
+  return cuda_status(e);
 }
 
 size_t ssd_cache_bytes(int n_keys) {

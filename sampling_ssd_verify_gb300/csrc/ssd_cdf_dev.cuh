@@ -317,6 +317,21 @@ __device__ __forceinline__ void load16(const CdfParams& p, const char* r, bool i
   }
 }
 
+// Saguaro row g's guesses: its top list minus the drawn token t, truncated
+// to the row's fan-out, padded with -1 to p.F columns.  One thread.
+__device__ __forceinline__ void write_guesses(const CdfParams& p, int64_t g, const RowResult* rr,
+                                              int t) {
+  const int F = p.F_rows ? min(max(__ldg(p.F_rows + g), 0), p.F) : p.F;
+  int n = 0;
+  for (int k = 0; k < kMaxTopK && n < F; ++k) {
+    const int i = __ldcg(&rr->ti[k]);
+    if (i < 0 || i == t) continue;
+    p.out_guess[g * p.F + n] = i;
+    ++n;
+  }
+  for (; n < p.F; ++n) p.out_guess[g * p.F + n] = -1;
+}
+
 // The draw for group g (one warp of the CTA that completes the group).
 // 1. Z = sum of the group's unit sums (each lane holds 16 units at once).
 // 2. The unit holding u*Z: lane prefix + warp scan, then inside the lane
@@ -475,17 +490,7 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
                   p.rc.branch, p.rc.all_hit, p.rc.cnt);
   if (p.out_mass) p.out_mass[g] = (float)Zd;
   if (p.out_qprime) p.out_qprime[g] = (float)((double)wt / Zd);
-  if (p.out_guess) {
-    const RowResult* rr = p.rowres + g * p.rpg + p.nt;
-    int n = 0;
-    for (int k = 0; k < kMaxTopK && n < p.F; ++k) {
-      const int i = __ldcg(&rr->ti[k]);
-      if (i < 0 || i == t) continue;
-      p.out_guess[g * p.F + n] = i;
-      ++n;
-    }
-    for (; n < p.F; ++n) p.out_guess[g * p.F + n] = -1;
-  }
+  if (p.out_guess) write_guesses(p, g, p.rowres + g * p.rpg + p.nt, t);
 }
 
 // Sum of the draw weights of one whole unit whose elements sit 16-byte
@@ -677,6 +682,222 @@ __device__ __forceinline__ void cdf_chunk_done(const CdfParams& p, int64_t g, in
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (last) group_draw<DT>(p, g);
+}
+
+
+// ---- one-term draws straight from the streaming pass ---------------------------------
+// The weight of a Saguaro row (q', [SSD-note] §"Saguaro 优化二") or of the
+// all-accepted bonus (p_K, [SD-7.3] §7.3.2) has one term, so the streaming
+// pass can sum it per block while the row goes by: bs[b] = (sum of
+// exp2(z*c - off) over block b, off).  Block b is consumer warp b % 16's
+// share of stage b / 16 of an aligned row: elements [s*E + w*BE, +BE).
+// The draw then needs only the block holding u*Z, read again from L2:
+//   W_b = bs[b].sum * 2^(off_b - mc) * scale (+ for a Saguaro set S, the
+//         difference of the in-S and out-of-S weights of its tokens in b),
+//   Z = sum_b W_b, the block where the prefix crosses u*Z, then the tokens
+//   of that block in vocabulary order.
+// Sums and prefixes are double-float pairs, as in group_draw.  One warp;
+// rr (Saguaro: the row's top list, null for p_K) gives S and the guesses.
+template <int DT>
+__device__ void direct_draw(const CdfParams& p, const float2* bs, int nblk, const GroupParams& gp,
+                            int64_t g, const RowResult* rr, int F) {
+  constexpr int R = 16;  // block sums per lane per round
+  constexpr int ES = Elem<DT>::kSize;
+  constexpr int VEC = Elem<DT>::kVec;
+  constexpr int BE = kVecsPerWarp * VEC;                 // elements per block
+  constexpr int E = units_per_stage(ES) * kUnitA;        // elements per stage
+  constexpr int PL = BE / 32;                            // elements per lane in a block
+  static_assert(PL % 16 == 0 && PL <= 32, "a lane's run is one or two 16-element halves");
+  const int lane = threadIdx.x & 31;
+  if (!SSD_CHK(g < p.groups, p.dbg, 50, g, p.groups)) return;
+  const bool tgt = gp.use_t != 0;
+  const float mc = tgt ? gp.mc_t : gp.mc_d;
+  const float sc = tgt ? gp.inv_st : gp.scale_out;
+  const bool has_s = !tgt && gp.theta != INFINITY && rr != nullptr;
+  const int nS = has_s ? F : 0;
+  const float dsc = gp.scale_in - gp.scale_out;
+  const char* row = tgt ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : row_ptr(p.dft, gp.row_d, p.d_stride, ES);
+  const int rounds = (nblk + 32 * R - 1) / (32 * R);
+  float v[R];
+  auto load_round = [&](int rnd) {
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const int b = rnd * 32 * R + lane * R + k;
+      float w = 0.f;
+      if (b < nblk) {
+        const float2 e = __ldcg(bs + b);
+        if (e.x > 0.f) w = e.x * ex2(e.y - mc) * sc;
+      }
+      v[k] = w;
+    }
+    // the cached set's tokens move from the out-of-S to the in-S weight
+    for (int f = 0; f < nS; ++f) {
+      const int tok = __ldcg(&rr->ti[f]);
+      if (tok < 0) continue;
+      const int b = (tok / E) * kConsumerWarps + (tok % E) / BE;
+      const int k = b - rnd * 32 * R - lane * R;
+      if (k >= 0 && k < R) {
+        const float d = dsc * ex2(fmaf(__ldcg(&rr->tv[f]), gp.c, -mc));
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+          if (q == k) v[q] = fmaxf(v[q] + d, 0.f);
+      }
+    }
+  };
+  load_round(0);
+  DF loc0 = df_sum16(v);
+  DF Zl = loc0;
+  for (int rnd = 1; rnd < rounds; ++rnd) {
+    load_round(rnd);
+    Zl = df_add(Zl, df_sum16(v));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const DF o{__shfl_xor_sync(0xffffffffu, Zl.hi, off), __shfl_xor_sync(0xffffffffu, Zl.lo, off)};
+    Zl = df_add(Zl, o);
+  }
+  const DF Z = Zl;
+  double Zd = (double)Z.hi + (double)Z.lo;
+  int t;
+  float wt;
+  if (!(Zd > 1e-30)) {
+    // a one-term weight sums to about 1; keep a defined result anyway
+    if (lane == 0 && p.status) atomicOr(p.status, SSD_DEV_ZERO_RESIDUAL);
+    t = full_row_draw<DT>(p, gp, tgt ? row : nullptr, tgt ? nullptr : row, &Zd);
+    wt = weight_global<DT>(p, gp, tgt ? row : nullptr, tgt ? nullptr : row, t);
+  } else {
+    const DF thr = df_scale(Z, (float)gp.u);
+    int blk = -1;
+    DF before{0.f, 0.f};
+    bool any_before = true;
+    DF run{0.f, 0.f};
+    for (int rnd = 0; rnd < rounds && blk < 0; ++rnd) {
+      DF loc = loc0;
+      if (rounds > 1) {
+        load_round(rnd);
+        if (rnd > 0) loc = df_sum16(v);
+      }
+      const DF incl = df_warp_scan(loc);
+      const DF up = df_shfl_up(incl, 1);
+      const DF excl = lane == 0 ? DF{0.f, 0.f} : up;
+      const unsigned m = __ballot_sync(0xffffffffu, df_gt(df_add(run, incl), thr));
+      if (m) {
+        const int L = __ffs(m) - 1;
+        const DF base = df_add(run, df_shfl(excl, L));
+        DF bk;
+        int lastk;
+        int uk = lane_search16(v, L, base, thr, &bk, &lastk);
+        if (uk < 0) {
+          uk = lastk;
+          any_before = false;
+        }
+        if (uk >= 0) {
+          blk = rnd * 32 * R + L * R + uk;
+          before = bk;
+        }
+      }
+      run = df_add(run, df_shfl(incl, 31));
+    }
+    if (blk < 0) {  // no prefix exceeded u*Z: the last block with weight
+      int cand = -1;
+      for (int rnd = 0; rnd < rounds; ++rnd) {
+        load_round(rnd);
+#pragma unroll
+        for (int k = 0; k < R; ++k)
+          if (v[k] > 0.f) cand = rnd * 32 * R + lane * R + k;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cand = max(cand, __shfl_xor_sync(0xffffffffu, cand, off));
+      blk = cand >= 0 ? cand : 0;
+      any_before = false;
+    }
+    // the block's tokens in vocabulary order: lane l holds PL consecutive ones
+    const int e_lo = (blk / kConsumerWarps) * E + (blk % kConsumerWarps) * BE;
+    const int e_hi = min(p.V, e_lo + BE);
+    const int y0 = e_lo + lane * PL;
+    float z[PL], w[PL];
+#pragma unroll
+    for (int k = 0; k < PL; k += VEC) {
+      const uintptr_t a = (uintptr_t)(row + (int64_t)(y0 + k) * ES);
+      uint4 r4 = make_uint4(0, 0, 0, 0);
+      const bool in = y0 + k + VEC <= e_hi &&
+                      SSD_CHK(in_range(a, a + 16, tgt ? p.t_lo : p.d_lo, tgt ? p.t_hi : p.d_hi),
+                              p.dbg, 51, y0 + k, g);
+      if (in) r4 = __ldg(reinterpret_cast<const uint4*>(a));
+      Elem<DT>::unpack(r4, z + k);
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) {
+        const int y = y0 + k + q;
+        float wy = 0.f;
+        if (in) {
+          const float e = ex2(fmaf(z[k + q], gp.c, -mc));
+          wy = tgt ? e * gp.inv_st : e * q_scale<true>(gp, y, z[k + q]);
+        }
+        w[k + q] = wy;
+      }
+    }
+    int lastpos = -1;
+#pragma unroll
+    for (int k = 0; k < PL; ++k)
+      if (w[k] > 0.f) lastpos = y0 + k;
+    DF lsum = df_sum16(w);
+    if constexpr (PL == 32) lsum = df_add(lsum, df_sum16(w + 16));
+    const DF incl = df_warp_scan(lsum);
+    const DF up = df_shfl_up(incl, 1);
+    const DF excl = lane == 0 ? DF{0.f, 0.f} : up;
+    t = -1;
+    const unsigned m = __ballot_sync(0xffffffffu, any_before && df_gt(df_add(before, incl), thr));
+    if (m) {
+      const int L = __ffs(m) - 1;
+      const DF base = df_add(before, df_shfl(excl, L));
+      DF bt;
+      int lastk;
+      int tk;
+      if constexpr (PL == 32) {
+        // the first half of lane L's run, then (if it does not cross) the second
+        const DF half = df_shfl(df_sum16(w), L);
+        if (df_gt(df_add(base, half), thr)) {
+          tk = lane_search16(w, L, base, thr, &bt, &lastk);
+          if (tk < 0) tk = lastk;
+        } else {
+          tk = lane_search16(w + 16, L, df_add(base, half), thr, &bt, &lastk);
+          if (tk < 0) tk = lastk;
+          if (tk >= 0) tk += 16;
+          else {  // rounding: the last positive weight of the first half
+            int lk2;
+            DF b2;
+            (void)lane_search16(w, L, base, thr, &b2, &lk2);
+            tk = lk2;
+          }
+        }
+      } else {
+        tk = lane_search16(w, L, base, thr, &bt, &lastk);
+        if (tk < 0) tk = lastk;
+      }
+      if (tk >= 0) t = e_lo + L * PL + tk;
+    }
+    if (t < 0) {  // rounding left no index: the last positive weight of the block
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
+      t = lastpos >= 0 ? lastpos : e_lo;
+    }
+    const int owner = (t - e_lo) / PL;
+    float wown = 0.f;
+#pragma unroll
+    for (int k = 0; k < PL; ++k)
+      if (y0 + k == t) wown = w[k];
+    wt = __shfl_sync(0xffffffffu, wown, owner & 31);
+  }
+  if (lane != 0) return;
+  if (!SSD_CHK(t >= 0 && t < p.V, p.dbg, 52, g, t)) return;
+  p.out_token[g] = t;
+  if (p.rc.table != nullptr)  // the round's cache: look the outcome (k, t) up
+    round_outcome(static_cast<const Slot*>(p.rc.table), p.rc.cap, g, gp.k, t, p.groups,
+                  p.rc.branch, p.rc.all_hit, p.rc.cnt);
+  if (p.out_mass) p.out_mass[g] = (float)Zd;
+  if (p.out_qprime) p.out_qprime[g] = (float)((double)wt / Zd);
+  if (p.out_guess && rr != nullptr) write_guesses(p, g, rr, t);
 }
 
 }  // namespace

@@ -133,6 +133,47 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Relaxed / acquire loads and release stores of 32-bit words that other
+// CTAs of the launch write (draw-queue counters and entries).
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* f) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* f) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_s32(int* f, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+// Atomic add / or with acquire-release semantics at GPU scope: the thread's
+// earlier writes (and those ordered before them) are published with the
+// update, and the writes published by earlier updates are visible after it.
+__device__ __forceinline__ int atom_add_acq_rel(int* f, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(f), "r"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_or_acq_rel(unsigned long long* f,
+                                                              unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(f), "l"(v)
+               : "memory");
+  return old;
+}
+
+// Warp-wide maximum of a float (redux.sync .f32, sm_100 family); -inf is an
+// ordinary value, NaN inputs are not expected.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // Named barrier over the consumer warps only (the producer warp never joins).
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");

@@ -1,6 +1,6 @@
 // ssd_internal.cuh -- shared definitions of the CUDA library (not part of
 // the public ABI): tuning constants, kernel parameter blocks, workspace
-// records and small device helpers (PTX wrappers, Philox, reductions).
+// records and the launcher declarations.
 //
 // Sources, cited by page title and section:
 //   [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈"
@@ -17,28 +17,41 @@ namespace ssd {
 // ---- tuning ------------------------------------------------------------------
 constexpr int kConsumerWarps = 16;                  // warps that reduce staged data
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;           // + one producer (bulk-copy) warp
 constexpr int kUnitA = 1024;                        // elements per work unit, streaming pass
 constexpr int kStageBytes = 32768;                  // bytes per pipeline stage
-constexpr int kStagesA = 6;                         // ring depth, streaming pass
-constexpr int kUnitB = 512;                         // elements per unit, CDF pass
-// units of the draws per stage of the streaming ring (target and draft runs
-// of kStageBytes / 2 each)
-__host__ __device__ constexpr int fused_units_per_stage(int esize) { return kStageBytes / 2 / (kUnitB * esize); }
+constexpr int kStagesA = 6;                         // ring depth
+constexpr int kStageVecs = kStageBytes / 16;        // 16-byte vectors per stage
+constexpr int kVecsPerWarp = kStageVecs / kConsumerWarps;  // one block: 128 vectors
+constexpr int kVpt = kVecsPerWarp / 32;             // vectors per consumer thread and stage
+constexpr int kUnitB = 512;                         // elements per unit of the draws
 constexpr int kMaxTopK = 16;                        // per-row candidate list (F + 1 <= 16)
+constexpr int kMaxChunkStages = 32;                 // stages of one row chunk (block maxima in smem)
+constexpr int kMaxBlocks = kMaxChunkStages * kConsumerWarps;
 constexpr int kMaxGrid = 4096;                      // bound on CTAs of one launch
-constexpr int kMaxChunks = 16;                      // bound on chunks per row (streaming pass)
+constexpr int kTokCache = 4096;                     // draft tokens kept in shared memory
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s
+
+// units of the draws per stage when both rows are read (target and draft
+// runs of kStageBytes / 2 each)
+__host__ __device__ constexpr int fused_units_per_stage(int esize) {
+  return kStageBytes / 2 / (kUnitB * esize);
+}
+// units of the streaming pass per stage
+__host__ __device__ constexpr int units_per_stage(int esize) {
+  return kStageBytes / (kUnitA * esize);
+}
 
 enum Mode : int { kModeVerify = 0, kModeTopF = 1, kModeSaguaro = 2 };
 
-// Per-(CTA, row piece) partial of the streaming pass.
+// Per-(row chunk) partial of the streaming pass, merged by the last chunk
+// of the row to finish.
 struct RowPartial {
-  float m;        // max raw logit of the piece
-  float pad;
+  float m;        // max raw logit of the chunk
+  float zx;       // logit of the row's draft token, when the chunk holds it
   float s_hi;     // sum of exp2(z*c - fl(m*c)) as a compensated pair
   float s_lo;
-  float tv[kMaxTopK];
+  int has_zx;
+  float tv[kMaxTopK];  // the chunk's exact top list (value desc, index asc)
   int ti[kMaxTopK];
 };
 
@@ -53,12 +66,12 @@ struct RowResult {
   int ti[kMaxTopK];
 };
 
-// Per-group (sequence / branch row) parameters of the CDF pass, written by
-// the group epilogue of the streaming pass.
+// Per-group (sequence / branch row) parameters of a draw, written by the
+// thread that decides the group's outcome.
 struct GroupParams {
-  int k;            // verify: accept length; rows read by the CDF pass: see below
-  int use_t;        // the CDF weight has a target term p(y)
-  int use_d;        // the CDF weight has a draft term q'(y)
+  int k;            // verify: accept length
+  int use_t;        // the draw weight has a target term p(y)
+  int use_d;        // the draw weight has a draft term q'(y)
   int sign_d;       // +1: w = q'(y) (Saguaro draw), -1: w = (p(y) - q'(y))^+
   int64_t row_t;    // target row index (into the target tensor)
   int64_t row_d;    // draft row index (into the draft tensor)
@@ -69,8 +82,7 @@ struct GroupParams {
   float c;          // log2(e) / T of the group
   double u;         // uniform of the draw
 };
-// A group whose outputs its epilogue already wrote (a greedy sequence): its
-// draw chunks do nothing.
+// A group whose outputs its epilogue already wrote (a greedy sequence): no draw.
 __host__ __device__ inline bool no_draw(const GroupParams& gp) { return !gp.use_t && !gp.use_d; }
 
 // The outcome cache of one round built and probed inside the verify launch
@@ -95,14 +107,19 @@ struct StreamParams {
   int B, K, Kq, V;
   int nt, nd, rpg;          // target rows, draft rows per group, rows per group
   int64_t NR;               // rows in total
-  int upr;                  // units per row
-  int64_t total_units;
-  // Rows are cut into nch chunks of clen units (the last one shorter); CTAs
-  // take chunks in the order (chunk of row, row) from a global counter.
+  int upr;                  // units (kUnitA elements) per row
+  int spr;                  // stages per row
+  int nblk;                 // blocks (one consumer warp's share of a stage) per row
+  // Rows are cut into nch chunks of clen units (a multiple of the stage
+  // length, the last one shorter); CTAs take chunks from a global counter.
+  // order 0: chunk c is (chunk c / NR of row c % NR); order 1 (verify):
+  // position-major -- for each draft position i, every sequence's target
+  // and draft rows of position i, so that outcomes are decided (and their
+  // draws run, from L2) while later positions stream.
   int nch, clen;
+  int order;
   int64_t nchunks;
   unsigned long long* chunk_ctr;
-  uint32_t* row_cut;        // per row: ordered-float lower bound on its top-list cut (0: none)
   float c;                  // log2(e) / T
   // Per-sequence temperature (device [B]) or null: then every sequence uses
   // T, greedy when greedy_all.  T = 0 is the greedy limit.
@@ -110,6 +127,7 @@ struct StreamParams {
   int greedy_all;
   float C[SSD_MAX_K + 1];   // Saguaro factor per draft position (a continuation draw: C[0])
   int F[SSD_MAX_K + 1];
+  const int32_t* F_rows;    // Saguaro: device [R] fan-out per row, or null: F[0]
   int need_top;             // draft rows keep a top list
   const int32_t* tokens;    // [groups, tokK] or null
   int tokK;
@@ -118,23 +136,33 @@ struct StreamParams {
   int jpos;                 // Saguaro: continuation position
   int mode;
   int32_t* accept_len;
-  int32_t* bonus;           // written by the epilogue of a greedy sequence
+  int32_t* bonus;           // written directly for greedy sequences and direct draws
   float* resid_mass;
   RoundCache rc;
   int32_t* guesses;         // [groups, nd, Fmax]
   float* guess_q;
   int Fmax;
-  int* row_cnt;
-  int* grp_cnt;
-  int* grp_ready;           // per group: 1 once its draw parameters are published
+  int* row_cnt;             // [NR] chunk arrivals of split rows
   RowPartial* partials;     // slot row * nch + chunk of row
-  // One-row draws whose unit sums the streaming pass writes (Saguaro rows,
-  // aligned): per 32-vector sub-unit of each row, (sum of exp2(z*c - off),
-  // off); null when the draws read the rows again.
-  float2* usum;
-  int nsu;                  // sub-units per row
   RowResult* rowres;
   GroupParams* gparams;
+  // One-row draws straight from the streaming pass (aligned rows: Saguaro
+  // rows, and target row K of a verified sequence): per (group, block) the
+  // sum of exp2(z*c - off) over the block and its offset off; null when
+  // those draws read their row again.
+  float2* bsum;
+  // Sequence outcomes (verify): per (sequence, position) arrivals of the
+  // position's rows, per sequence the state word (bit i: position i
+  // accepted, bit 32 + i: rejected) and the all-accepted counter.
+  int* pair_cnt;
+  unsigned long long* seq_state;
+  int* kcnt;
+  // Draw queue: a decided group's chunks are pushed as tickets (entry =
+  // chunk id + 1, 0 while unwritten); producers claim tickets in order.
+  int* dq_entry;
+  unsigned int* dq_tail;
+  unsigned int* dq_head;
+  int* decided;             // groups whose draw is queued or done
   int32_t* status;
   // bounds of the inputs and the debug record (used by SSD_CHECKS builds)
   const char* t_lo;
@@ -152,7 +180,7 @@ struct CdfParams {
   int groups, V, nsub;
   int64_t total_units;
   // Each group's nsub units are cut into cpg chunks of cu units (the last one
-  // shorter), taken group by group.
+  // shorter); chunk id = group * cpg + chunk.
   int cu, cpg;
   int64_t nchunks;
   int mode;
@@ -164,8 +192,9 @@ struct CdfParams {
   int32_t* out_token;
   float* out_mass;          // verify: resid mass
   float* out_qprime;        // Saguaro: q'(x)
-  int32_t* out_guess;       // Saguaro: [groups, F]
-  int F;
+  int32_t* out_guess;       // Saguaro: [groups, Fmax]
+  int F;                    // Saguaro: Fmax (columns of out_guess)
+  const int32_t* F_rows;    // Saguaro: per-row fan-out, or null: F
   RoundCache rc;
   int32_t* status;
   const char* t_lo;
@@ -175,58 +204,98 @@ struct CdfParams {
   unsigned long long* dbg;
 };
 
-// The streaming pass and the draws in one persistent launch: logical chunks
-// [0, s.nchunks) stream rows, [s.nchunks, s.nchunks + q.nchunks) are chunks
-// of the draws (none when q.nchunks is 0), all taken from the one counter
-// s.chunk_ctr.  A chunk of the draws waits until its group's
-// parameters are published (s.grp_ready), so the launch is cooperative.
+// The streaming pass and the draws in one persistent launch: row chunks
+// [0, s.nchunks) from the counter s.chunk_ctr, draw chunks from the ticket
+// queue as groups are decided.  CTAs wait for one another (draw tickets,
+// split rows, the round cache), so the launch is cooperative.
 struct VerifyParams {
   StreamParams s;
   CdfParams q;
 };
 
+// Tree-draft verification (ssd_tree.cu): one CTA per tree walks it after
+// the streaming pass has normalised every row (row u of tree b: target at
+// rowres[b * 2N + u], draft at rowres[b * 2N + N + u]).
+constexpr int kMaxTreeNodes = 256;
+struct TreeParams {
+  int B, N, V;
+  float c;                  // log2(e) / T
+  const void* tgt;
+  int64_t t_stride;
+  const void* dft;
+  int64_t d_stride;
+  const int32_t* tokens;    // [B, N]
+  const uint64_t* seeds;
+  uint32_t round;
+  const RowResult* rowres;
+  GroupParams* gparams;     // [B]
+  // children of node u: child[child_off[u] .. child_off[u+1]), in index order
+  int child_off[kMaxTreeNodes + 1];
+  int child[kMaxTreeNodes];
+  int32_t* accept_len;
+  int32_t* path;            // [B, Dmax] or null
+  int Dmax;
+  float* resid_mass;
+  int32_t* status;
+  CdfParams q;              // the bonus draw (unit sums, group_draw)
+};
+
 // ---- workspace layout ----------------------------------------------------------
 struct WsLayout {
   size_t cnt_off, cnt_bytes;       // counters (cleared each call)
-  size_t ctr_off;                  // the chunk counter, within the counters
-  size_t part_off, rowres_off, gp_off, sub_off, usum_off, dbg_off, total;
+  size_t ctr_off;                  // the 8-byte counters, within the counters
+  size_t part_off, rowres_off, gp_off, sub_off, bsum_off, dbg_off, total;
+  // offsets (in ints) of the int counters
+  size_t o_row_cnt, o_grp_cnt, o_pair, o_kcnt, o_dq, o_state;
   int64_t NR;
-  int groups, nsub;
+  int groups, nsub, nblk, cpg;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// nch: chunks per row of the streaming pass; split rows (nch > 1) need one
-// partial slot per chunk.  usum: room for the streaming pass's sub-unit sums
-// of every row (sub-units of at least 128 elements).
-inline WsLayout ws_layout(int groups, int rpg, int V, int nch, bool usum = false) {
+// groups of rpg rows (nt target rows, K positions), V elements per row of
+// esize bytes, nch chunks per row, cpg draw chunks per group; bsum: room for
+// the one-row draws' block sums (one row per group).
+inline WsLayout ws_layout(int groups, int rpg, int K, int V, int esize, int nch, int cpg,
+                          bool bsum) {
   WsLayout L;
   L.groups = groups;
   L.NR = (int64_t)groups * rpg;
   L.nsub = (V + kUnitB - 1) / kUnitB;
-  // counters: row arrivals [NR], group arrivals [groups], CDF arrivals
-  // [groups], row cuts [NR], group-ready flags [groups], then 8-byte
-  // counters: chunks, round-cache outcomes, round-cache clearing
-  size_t ncnt = 2 * (size_t)L.NR + 3 * (size_t)groups;
+  const int ups = units_per_stage(esize);
+  const int upr = (V + kUnitA - 1) / kUnitA;
+  L.nblk = ((upr + ups - 1) / ups) * kConsumerWarps;
+  L.cpg = cpg;
+  // int counters: row arrivals [NR], draw arrivals [groups], position
+  // arrivals [groups * (K+1)], all-accepted events [groups], draw tickets
+  // [groups * cpg]; then 8-byte words: sequence states [groups], the chunk
+  // counter, round-cache outcomes, round-cache clearing, queue tail / head,
+  // decided groups
+  L.o_row_cnt = 0;
+  L.o_grp_cnt = L.o_row_cnt + (size_t)L.NR;
+  L.o_pair = L.o_grp_cnt + (size_t)groups;
+  L.o_kcnt = L.o_pair + (size_t)groups * (K + 1);
+  L.o_dq = L.o_kcnt + (size_t)groups;
+  const size_t nint = L.o_dq + (size_t)groups * cpg;
   L.cnt_off = 0;
-  L.ctr_off = (ncnt * sizeof(int) + 7) & ~(size_t)7;
-  // chunk counter, round-cache outcomes, round-cache clearing
-  L.cnt_bytes = align256(L.ctr_off + 3 * sizeof(unsigned long long));
+  L.o_state = ((nint * sizeof(int) + 7) & ~(size_t)7) / 8;  // in 8-byte words
+  L.ctr_off = (L.o_state + (size_t)groups) * 8;
+  L.cnt_bytes = align256(L.ctr_off + 6 * sizeof(unsigned long long));
   L.part_off = L.cnt_bytes;
   const size_t slots = nch > 1 ? (size_t)L.NR * nch : 1;
   L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));
   L.gp_off = L.rowres_off + align256((size_t)L.NR * sizeof(RowResult));
   L.sub_off = L.gp_off + align256((size_t)groups * sizeof(GroupParams));
-  L.usum_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));
-  const size_t usum_bytes = usum ? (size_t)L.NR * ((V + 127) / 128) * 2 * sizeof(float) : 0;
-  L.dbg_off = L.usum_off + align256(usum_bytes);
+  L.bsum_off = L.sub_off + align256((size_t)groups * L.nsub * sizeof(float));
+  const size_t bsum_bytes = bsum ? (size_t)groups * L.nblk * sizeof(float2) : 0;
+  L.dbg_off = L.bsum_off + align256(bsum_bytes);
   L.total = L.dbg_off + 256;  // bounds-check record of SSD_CHECKS builds
   return L;
 }
 
-// ---- launchers (defined in ssd_stream.cu / ssd_cdf.cu / ssd_cache.cu) -----------
-cudaError_t launch_stream(const VerifyParams& p, int dtype, int topk, int grid,
-                          cudaStream_t s);
+// ---- launchers (ssd_stream_*.cu / ssd_cache.cu) ----------------------------------
+template <int DT>
+cudaError_t launch_stream_dt(const VerifyParams& p, int grid, cudaStream_t s);
 cudaError_t launch_cache_clear(void* table, int64_t capacity, cudaStream_t s);
 cudaError_t launch_cache_insert(void* table, int64_t capacity, const int32_t* row,
                                 const int32_t* k, const int32_t* t, const int32_t* branch, int n,
@@ -235,6 +304,8 @@ cudaError_t launch_cache_insert(void* table, int64_t capacity, const int32_t* ro
 cudaError_t launch_cache_lookup(const void* table, int64_t capacity, const int32_t* accept_len,
                                 const int32_t* bonus, int B, int32_t* out_branch,
                                 int32_t* all_hit, cudaStream_t s);
+template <int DT>
+cudaError_t launch_tree_dt(const TreeParams& tp, cudaStream_t s);
 int stream_smem_bytes();
 int num_sms();
 

@@ -12,8 +12,9 @@
 //
 // Set-up: the array's device address is looked up with cudaGetSymbolAddress
 // the first time the entry point runs on a device (with that device current)
-// and cached per device; that first call should therefore come before any
-// stream capture on the device.
+// and cached per device and context; that first call should therefore come
+// before any stream capture on the device.  After cudaDeviceReset (a new
+// context) the next call looks the address up again.
 //
 // Sharing: every call on a device uses the same array.  The counters that
 // must start at zero are cleared on the caller's stream at the start of each
@@ -36,9 +37,37 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+struct Cached {
+  void* ctx;  // the context the address belongs to
+  void* ptr;
+};
+Cached g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (cached).
+// The calling thread's current CUDA context (the driver's cuCtxGetCurrent,
+// reached through the runtime's entry-point query), or null.  A device reset
+// or a re-created primary context loads the library's module again, and the
+// array may then sit at another address: the cache is keyed on the context.
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    looked = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+    else
+      cudaGetLastError();
+  }
+  void* ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// Device address of the scratch array in the current context (cached).
 ssd_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -47,15 +76,18 @@ ssd_status scratch_for_current_device(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return SSD_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  void* ctx = current_context();
+  Cached& c = g_scratch[dev];
+  if (c.ptr == nullptr || ctx == nullptr || c.ctx != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();
       return SSD_ERR_CUDA;
     }
-    g_scratch_ptr[dev] = ptr;
+    c.ptr = ptr;
+    c.ctx = current_context();  // the query made the context current if it was not
   }
-  *out = g_scratch_ptr[dev];
+  *out = c.ptr;
   return SSD_OK;
 }
 

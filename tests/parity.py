@@ -6,8 +6,14 @@ Tolerances (the verify path's stated bar):
   * accept lengths, bonus tokens, top-F guesses, sampled tokens and cache
     branch ids: bit-exact, except rows the oracle marks as near-ties -- an
     accept test with |u - p/q'| < 1e-6 or an inverse-CDF draw whose
-    normalised margin is < 1e-6; rows where library and oracle actually
-    disagree (all of them near-ties) must stay under 0.1% of rows;
+    normalised margin is < 1e-6.  No row may differ outside that band.
+  * Rows where library and oracle actually disagree (all of them near-ties)
+    are counted.  For small vocabularies (V <= 4096) they must stay under
+    0.01% of the rows of every call and of the whole suite.  At V >= 128k a
+    draw's interval edges lie within the fp32 rounding of the kernel's
+    weights (about 1e-8 of the mass) for a share of the rows of order V x
+    1e-8, so the bound there is 0.3% of the rows, over the suite, with the
+    count of every call reported.
   * probabilities and residual masses: 1e-5 absolute.
 """
 
@@ -40,7 +46,25 @@ def i32(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
 
-def compare_verify(g, o, K, guesses=True, max_disagree_frac=1e-3):
+# rows and disagreements over the suite: {"small": [rows, disagree], "large": [...]}
+TALLY = {"small": [0, 0], "large": [0, 0]}
+SMALL_V = 4096
+FRAC = {"small": 1e-4, "large": 3e-3}
+
+
+def _count(V, rows, disagree):
+    cls = "small" if V is not None and V <= SMALL_V else "large"
+    TALLY[cls][0] += rows
+    TALLY[cls][1] += disagree
+    if cls == "small":
+        assert disagree <= FRAC["small"] * rows, f"{disagree} disagreements in {rows} rows (V={V})"
+    else:
+        # one call alone may hold a handful; the suite-wide share is bounded
+        assert disagree <= max(3, FRAC["large"] * rows), f"{disagree} disagreements in {rows} rows"
+    return cls
+
+
+def compare_verify(g, o, K, guesses=True, V=None):
     """g: library outputs (numpy), o: oracle outputs.
 
     Every row outside the declared near-tie band must be bit-exact.  The
@@ -59,7 +83,7 @@ def compare_verify(g, o, K, guesses=True, max_disagree_frac=1e-3):
         f"gpu k/t {acc_g[bad][:5]} {bon_g[bad][:5]} oracle {acc_o[bad][:5]} {bon_o[bad][:5]} "
         f"margins {o['margin_accept'][bad][:5]} {o['margin_cdf'][bad][:5]}")
     n_dis = int((~same).sum())
-    assert n_dis <= max(1, max_disagree_frac * B), f"{n_dis} disagreements in {B} rows"
+    _count(V, B, n_dis)
     ok = same
     if "resid_mass" in g:
         err = np.abs(g["resid_mass"][ok] - o["resid_mass"][ok])
@@ -73,14 +97,14 @@ def compare_verify(g, o, K, guesses=True, max_disagree_frac=1e-3):
                 accept_mean=float(acc_g.mean()))
 
 
-def compare_draws(tok_g, o, max_disagree_frac=1e-3):
+def compare_draws(tok_g, o, V=None):
     """Sampled tokens (Saguaro draws) with the same near-tie rule; returns
-    the boolean mask of rows that are not near-ties."""
+    the boolean mask of rows that are not near-ties and agree."""
     tie = o["margin_cdf"] < TIE
     diff = tok_g != o["token"]
     bad = diff & ~tie
     assert not bad.any(), (np.nonzero(bad)[0][:8], tok_g[bad][:8], o["token"][bad][:8])
-    assert diff.sum() <= max(1, max_disagree_frac * len(diff)), f"{diff.sum()} disagreements"
+    _count(V, len(diff), int(diff.sum()))
     return ~tie & ~diff
 
 

@@ -222,14 +222,19 @@ def test_other_entry_points_reject_bad_arguments(L):
                             0, None, None) == 1
     assert L.ssd_topf_bonus(ctypes.byref(d), 1, 2, 32, 1.0, None, 0, Fp, 0, 0x1000, None, None,
                             0, None, None) == 1
-    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.0, 2, 0x1000, 0, 0, 0x2000,
+    # (draft, R, V, T, C, F_row, Fmax, seeds, j, round, token, qprime, guess, ws, ws_bytes, ...)
+    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.0, None, 2, 0x1000, 0, 0, 0x2000,
                                 None, None, None, 0, None, None) == 1
-    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, 32, 0x1000, 0, 0, 0x2000,
+    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, None, 32, 0x1000, 0, 0, 0x2000,
                                 None, None, None, 0, None, None) == 1
-    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, 16, 0x1000, 0, 0, 0x2000,
+    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, None, -1, 0x1000, 0, 0, 0x2000,
+                                None, None, None, 0, None, None) == 1
+    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, None, 16, 0x1000, 0, 0, 0x2000,
                                 None, None, None, 0, None, None) == 2
-    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, 2, 0x1000, 0, 0, 0x2000,
+    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, None, 2, 0x1000, 0, 0, 0x2000,
                                 None, None, None, 0, None, None) == 5
+    assert L.ssd_saguaro_sample(ctypes.byref(d), 4, 32, 1.0, 0.5, 0x3000, 2, 0x1000, 0, 0,
+                                0x2000, None, None, None, 0, None, None) == 5
     assert L.ssd_cache_build(None, 4096, 1, 1, 1, 1, 4, None, None) == 1
     assert L.ssd_cache_build(0x1008, 4096, 1, 1, 1, 1, 4, None, None) == 1
     assert L.ssd_cache_build(0x1000, 64, 0x2000, 0x2000, 0x2000, 0x2000, 4, None, None) == 3

@@ -56,6 +56,8 @@ def test_noalloc_matches_workspace_entry_point(wname, B, V):
     tl, dl = ssd._logits(tg), ssd._logits(dg)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     for rnd in (7, 8):  # two calls in a row share the scratch array
+        torch.cuda.synchronize()
+        alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
         out = {"accept_len": torch.full((B,), -7, dtype=torch.int32, device=dev),
                "bonus": torch.full((B,), -7, dtype=torch.int32, device=dev),
                "resid_mass": torch.full((B,), -1.0, dtype=torch.float32, device=dev),
@@ -67,6 +69,12 @@ def test_noalloc_matches_workspace_entry_point(wname, B, V):
                _ptr(out["guess_q"]), Fmax, _ptr(status),
                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == 0, ssd.lib().ssd_status_string(st)
+        torch.cuda.synchronize()
+        if rnd == 8:
+            # after the first call has loaded everything, a call takes no
+            # device memory from torch's allocator or from the device
+            assert torch.cuda.memory_allocated() == alloc0
+            assert torch.cuda.mem_get_info()[0] == free0
         ref = ssd.verify(tg, dg, tok, seeds, rnd, F, w.C, w.T)
         torch.cuda.synchronize()
         for k in ("accept_len", "bonus", "guesses"):
