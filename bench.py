@@ -558,10 +558,11 @@ def run_fanout_ablation(args):
 
     w = WORKLOADS[args.workload]
     budget = int(sum(w.fanout))
-    rows = fanout_ablation(w, (0.5, 0.7, 1.0, 1.3, 1.6, 2.0), budget, Cs=sorted({1.0, w.C}),
-                           rounds=4, B=args.batch or None, V=args.vocab or None)
+    rounds = args.rounds
+    rows = fanout_ablation(w, (0.5, 0.7, 1.0, 1.3, 1.6), budget, Cs=sorted({1.0, w.C}),
+                           rounds=rounds, B=args.batch or None, V=args.vocab or None)
     print(json.dumps({"ablation": "fanout", "workload": w.name, "budget": budget,
-                      "B": args.batch or w.B, "V": args.vocab or w.V, "rounds": 4,
+                      "B": args.batch or w.B, "V": args.vocab or w.V, "rounds": rounds,
                       "data": "synthetic", "rows": rows}))
 
 
@@ -580,6 +581,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rounds", type=int, default=64, help="rounds per ablation cell")
     ap.add_argument("--ablation", choices=["fanout"], default=None,
                     help="instead of the benchmark: geometric vs uniform fan-out hit rates")
     args = ap.parse_args()

@@ -32,17 +32,9 @@ def uniform_fanout(K: int, budget: int) -> np.ndarray:
     return F
 
 
-def round_hits(workload, F, C, T, seed, rnd, device="cuda"):
-    """One synthetic round of B sequences: drafts x_j ~ q'_j, verification,
-    cache of every position's guesses, lookup of (k, t).  Returns the host
-    arrays accept_len, bonus, hit (bool per row) and the device outputs."""
+def _upload(bt, w, device):
     import torch
 
-    from ssd_inputs import make_batch
-
-    w = workload
-    bt = make_batch(w, seed=seed)
-    K = w.K
     if w.dtype == "bf16":
         tg = torch.from_numpy(bt["target"].view(np.int16)).to(device).view(torch.bfloat16)
         dg = torch.from_numpy(bt["draft"].view(np.int16)).to(device).view(torch.bfloat16)
@@ -50,9 +42,18 @@ def round_hits(workload, F, C, T, seed, rnd, device="cuda"):
         tg = torch.from_numpy(bt["target"]).to(device)
         dg = torch.from_numpy(bt["draft"]).to(device)
     seeds = torch.from_numpy(bt["seeds"].view(np.int64)).to(device)
+    return tg, dg, seeds
+
+
+def _round_on_device(tg, dg, seeds, K, F, C, T, rnd, device):
+    """Drafts x_j ~ q'_j (Saguaro sampling), verification with the guesses of
+    every position, the outcome cache of the guesses and its lookup."""
+    import torch
+
     F = np.asarray(F, dtype=np.int32)
     Cv = np.broadcast_to(np.asarray(C, dtype=np.float32), (K,))
-    tok = torch.empty((w.B, K), dtype=torch.int32, device=device)
+    B = tg.shape[0]
+    tok = torch.empty((B, K), dtype=torch.int32, device=device)
     for j in range(K):
         tok[:, j] = saguaro_sample(dg[:, j, :], T, float(Cv[j]), int(F[j]), seeds, j, rnd,
                                    guesses=False, qprime=False)["token"]
@@ -61,35 +62,75 @@ def round_hits(workload, F, C, T, seed, rnd, device="cuda"):
     table = torch.empty(cache_bytes(out["guesses"].numel()), dtype=torch.uint8, device=device)
     cache_build_guesses(out["guesses"], table=table)
     look = cache_lookup(table, out["accept_len"], out["bonus"])
+    return tok, out, look
+
+
+def round_hits(workload, F, C, T, seed, rnd, device="cuda"):
+    """One synthetic round of B sequences: drafts x_j ~ q'_j, verification,
+    cache of every position's guesses, lookup of (k, t).  Returns the host
+    arrays accept_len, bonus, hit (bool per row) and the device outputs."""
+    from ssd_inputs import make_batch
+
+    w = workload
+    bt = make_batch(w, seed=seed)
+    tg, dg, seeds = _upload(bt, w, device)
+    tok, out, look = _round_on_device(tg, dg, seeds, w.K, F, C, T, rnd, device)
     return dict(accept_len=out["accept_len"].cpu().numpy(), bonus=out["bonus"].cpu().numpy(),
                 hit=look["branch"].cpu().numpy() >= 0, tokens=tok.cpu().numpy(),
                 guesses=out["guesses"].cpu().numpy(), batch=bt)
 
 
-def fanout_ablation(workload, temperatures, budget, Cs=(1.0,), rounds=4, a=0.7, r=1.0,
+def wilson(h, n, z=1.96):
+    """Wilson score interval of a binomial proportion h / n."""
+    if n == 0:
+        return (0.0, 1.0)
+    p = h / n
+    d = 1 + z * z / n
+    c = (p + z * z / (2 * n)) / d
+    r = z * np.sqrt(p * (1 - p) / n + z * z / (4 * n * n)) / d
+    return (max(0.0, c - r), min(1.0, c + r))
+
+
+def fanout_ablation(workload, temperatures, budget, Cs=(1.0,), rounds=64, a=0.7, r=1.0,
                     B=None, V=None, seed=2024, device="cuda"):
     """Hit rate of the geometric allocation (a, r) and of the uniform one for
-    every (C, T), over `rounds` seeded rounds of B sequences each.  Returns a
-    list of dicts: C, T, F_geometric, F_uniform, hit_geometric, hit_uniform,
-    accept_mean (mean accepted drafts per row, geometric arm)."""
+    every (C, T), over `rounds` seeded rounds of B sequences each.  Each
+    round's logits are generated once and shared by every (C, T) and both
+    allocations, so the two arms are compared on the same sequences and
+    uniforms (paired).  Returns a list of dicts: C, T, F_geometric,
+    F_uniform, hit_geometric, hit_uniform (with 95% Wilson intervals),
+    diff = hit_geometric - hit_uniform with a 95% interval of the paired
+    per-row differences, rows, accept_mean (geometric arm)."""
+    from ssd_inputs import make_batch
+
     w = dataclasses.replace(workload, B=B or workload.B, V=V or workload.V)
     Fg = fanout(w.K, budget, a, r)
     Fu = uniform_fanout(w.K, budget)
-    rows = []
-    for C in Cs:
-        for T in temperatures:
-            wt = dataclasses.replace(w, T=float(T), C=float(C))
-            hits = {"geometric": 0, "uniform": 0}
-            acc = 0.0
-            n = 0
-            for i in range(rounds):
+    cells = {(C, T): {"geometric": [], "uniform": [], "acc": []} for C in Cs for T in temperatures}
+    for i in range(rounds):
+        bt = make_batch(w, seed=seed + i)
+        tg, dg, seeds = _upload(bt, w, device)
+        for C in Cs:
+            for T in temperatures:
+                cell = cells[(C, T)]
                 for name, F in (("geometric", Fg), ("uniform", Fu)):
-                    res = round_hits(wt, F, C, T, seed + i, i, device)
-                    hits[name] += int(res["hit"].sum())
+                    _, out, look = _round_on_device(tg, dg, seeds, w.K, F, C, float(T), i,
+                                                    device)
+                    cell[name].append(look["branch"].cpu().numpy() >= 0)
                     if name == "geometric":
-                        acc += float(res["accept_len"].sum())
-                        n += len(res["hit"])
-            rows.append(dict(C=float(C), T=float(T), F_geometric=Fg.tolist(),
-                             F_uniform=Fu.tolist(), hit_geometric=hits["geometric"] / n,
-                             hit_uniform=hits["uniform"] / n, accept_mean=acc / n))
+                        cell["acc"].append(out["accept_len"].cpu().numpy())
+    rows = []
+    for (C, T), cell in cells.items():
+        hg = np.concatenate(cell["geometric"])
+        hu = np.concatenate(cell["uniform"])
+        n = len(hg)
+        d = hg.astype(np.float64) - hu.astype(np.float64)
+        half = 1.96 * d.std(ddof=1) / np.sqrt(n) if n > 1 else 1.0
+        rows.append(dict(C=float(C), T=float(T), F_geometric=Fg.tolist(), F_uniform=Fu.tolist(),
+                         rows=n, hit_geometric=float(hg.mean()),
+                         hit_geometric_ci=wilson(int(hg.sum()), n),
+                         hit_uniform=float(hu.mean()), hit_uniform_ci=wilson(int(hu.sum()), n),
+                         diff=float(d.mean()), diff_ci=(float(d.mean() - half),
+                                                        float(d.mean() + half)),
+                         accept_mean=float(np.concatenate(cell["acc"]).mean())))
     return rows

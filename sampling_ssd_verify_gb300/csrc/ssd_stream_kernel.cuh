@@ -72,6 +72,7 @@ static_assert(kPieceSlots % kEpilogueWarps == 0, "a slot belongs to one epilogue
 // The producer runs at most kStagesA + 1 pieces ahead of the consumer
 // warps, so a descriptor queue this long is never overwritten early.
 constexpr int kPieceQueue = 16;
+constexpr int kMaxCand = 64;  // top-list candidates a piece hands to its epilogue
 static_assert(kPieceQueue > kStagesA + 1, "piece queue shorter than the pipeline");
 
 struct alignas(16) PieceRed {
@@ -84,6 +85,12 @@ struct alignas(16) PieceRed {
   float lo[kConsumerWarps];
   float wmax[kConsumerWarps];  // each consumer warp's largest logit of the piece
   float bmax[kMaxBlocks];  // block maxima, (stage of the piece) * kConsumerWarps + warp
+  // The piece's top-list candidates: every logit >= theta of the blocks
+  // whose maximum reaches theta, found by the consumer warps at the end of
+  // the piece (ncand > kMaxCand: too many, the epilogue reads the blocks).
+  int ncand;
+  float cand_v[kMaxCand];
+  int cand_i[kMaxCand];
 };
 
 // Geometry of one pipeline stage: the element range [e0, e1) of row `row`
@@ -440,6 +447,73 @@ __device__ __forceinline__ void reread_block(const StreamParams& p, const char* 
           x = Elem<DT>::load_cg(reinterpret_cast<const void*>(st.b0), (int64_t)(idx - st.e0));
       }
       wl.offer(x, idx, x >= th);
+    }
+  }
+}
+
+// Consumer warp wb lists the logits >= th of its block of stage s (read
+// again from global memory) in the piece's candidate list.
+template <int DT>
+__device__ __forceinline__ void list_block(const StreamParams& p, const char* rp, bool is_t, int s,
+                                           int wb, float th, int64_t row, PieceRed& R) {
+  constexpr int VEC = Elem<DT>::kVec;
+  const int lane = threadIdx.x & 31;
+  const char* lo = is_t ? p.t_lo : p.d_lo;
+  const char* hi = is_t ? p.t_hi : p.d_hi;
+  (void)lo;
+  (void)hi;  // read by the bounds-checked build only
+  const Stage st = stage_of<DT>(rp, p.V, s);
+  const int nvec = (int)((st.a1 - st.a0) >> 4);
+  const int ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
+  uint4 raw[kVpt];
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    const int vi = wb * kVecsPerWarp + lane + 32 * k;
+    const uintptr_t a = st.a0 + (uintptr_t)vi * 16;
+    raw[k] = make_uint4(0, 0, 0, 0);
+    if (vi < nvec && SSD_CHK(in_range(a, a + 16, lo, hi), p.dbg, 32, row, vi))
+      raw[k] = __ldg(reinterpret_cast<const uint4*>(a));
+  }
+  auto put = [&](float x, int idx, bool ok) {
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    if (!m) return;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&R.ncand, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(m & ((1u << lane) - 1u));
+    if (ok && pos < kMaxCand) {
+      R.cand_v[pos] = x;
+      R.cand_i[pos] = idx;
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < kVpt; ++k) {
+    const int vi = wb * kVecsPerWarp + lane + 32 * k;
+    float x[VEC];
+    Elem<DT>::unpack(raw[k], x);
+    float vm = x[0];
+#pragma unroll
+    for (int e = 1; e < VEC; ++e) vm = fmaxf(vm, x[e]);
+    if (!__any_sync(0xffffffffu, vi < nvec && vm >= th)) continue;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) put(x[e], ei0 + vi * VEC + e, vi < nvec && x[e] >= th);
+  }
+  if (wb == 0) {
+    // the stage's unaligned head and tail
+    const int hc = nvec > 0 ? ei0 - st.e0 : st.e1 - st.e0;
+    const int ei1 = ei0 + nvec * VEC;
+    const int tc = nvec > 0 ? st.e1 - ei1 : 0;
+    for (int f0 = 0; f0 < hc + tc; f0 += 32) {
+      const int f = f0 + lane;
+      float x = kNegInf;
+      int idx = 0;
+      if (f < hc + tc) {
+        idx = f < hc ? st.e0 + f : ei1 + (f - hc);
+        const uintptr_t fa = st.b0 + (uintptr_t)(idx - st.e0) * Elem<DT>::kSize;
+        if (SSD_CHK(in_range(fa, fa + Elem<DT>::kSize, lo, hi), p.dbg, 33, row, idx))
+          x = Elem<DT>::load(reinterpret_cast<const void*>(st.b0), (int64_t)(idx - st.e0));
+      }
+      put(x, idx, x != kNegInf && x >= th);
     }
   }
 }
@@ -1131,6 +1205,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         v[j] = (need > 0 && bb < nb) ? R.bmax[bb] : kNegInf;
       }
       const float wmx = (need > 0 && lane < kConsumerWarps) ? R.wmax[lane] : kNegInf;
+      const int ncand = need > 0 ? R.ncand : 0;
+      float cvv[kMaxCand / 32];
+      int cvi[kMaxCand / 32];
+#pragma unroll
+      for (int q = 0; q < kMaxCand / 32; ++q) {
+        const int i = q * 32 + lane;
+        cvv[q] = i < ncand && i < kMaxCand ? R.cand_v[i] : kNegInf;
+        cvi[q] = i < ncand && i < kMaxCand ? R.cand_i[i] : 0;
+      }
       // the row's draft token and, when this piece holds it, its logit
       const int jx = jr < p.nt ? jr : jr - p.nt;
       const int x = (tok_smem && jx < p.tokK) ? s_tok[g * p.tokK + jx] : -1;
@@ -1143,7 +1226,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       warp_softmax_merge(b.m, b.mc, b.hi, b.lo, c, M, MC, Shi, Slo);
       WarpList wl;
       wl.reset(need > 0 ? need : 1);
-      if (need > 0) chunk_top<DT>(p, row, (int)((pu0 - row * p.upr) / (int64_t)ups), wmx, v, wl);
+      if (need > 0) {
+        if (ncand <= kMaxCand) {
+          // the candidates the consumer warps listed
+          for (int i0 = 0; i0 < ncand; i0 += 32) {
+            const bool ok = i0 + lane < ncand;
+            wl.offer(ok ? cvv[i0 / 32] : kNegInf, ok ? cvi[i0 / 32] : 0, ok);
+          }
+        } else {
+          chunk_top<DT>(p, row, (int)((pu0 - row * p.upr) / (int64_t)ups), wmx, v, wl);
+        }
+      }
       if (p.nch == 1) {
         finalize_row<DT>(p, cq, row, c, M, MC, Shi, Slo, wl, need, x >= 0, x, zx, &cleared,
                          &s_err);
@@ -1280,6 +1373,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int xtok = (tok_smem && jx < p.tokK) ? s_tok[g * p.tokK + jx] : -1;
     a.reset();
     float wmax = kNegInf;  // this warp's largest logit of the piece
+    float mybm = kNegInf;  // lane s: this warp's block maximum of stage s of the piece
+    if (top && warp == 0 && lane == 0) R.ncand = 0;
     const int nst = (int)((pu1 - pu0 + ups - 1) / ups);  // stages of the piece
     for (int s = 0; s < nst; ++s) {
       if (s != 0) mbar_wait(full + slot, phase, &s_err, p.status);
@@ -1351,6 +1446,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if (top) {
         const float bm = warp_max_f32(vm);
         wmax = fmaxf(wmax, bm);
+        if (lane == s) mybm = bm;
         if (lane == 0) R.bmax[s * kConsumerWarps + warp] = bm;
       }
       if (xtok >= 0 && lane == 0) {
@@ -1367,11 +1463,36 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       }
     }
 
+    if (top) {
+      // The piece's top-list candidates.  theta = the R-th largest of the 16
+      // warp maxima (R warps hold a logit >= theta, so no logit below it is
+      // in the top R); each warp reads its own blocks whose maximum reaches
+      // theta again (from L2, just streamed) and lists their logits >= theta.
+      if (lane == 0) R.wmax[warp] = wmax;
+      consumer_sync();
+      float m = lane < kConsumerWarps ? R.wmax[lane] : kNegInf;
+      float th = kNegInf;
+      for (int r = 0; r < d.need; ++r) {
+        const float mx = warp_max_f32(m);
+        if (mx == kNegInf) {
+          th = kNegInf;
+          break;
+        }
+        th = mx;
+        const unsigned who = __ballot_sync(0xffffffffu, m == mx);
+        if (lane == __ffs(who) - 1) m = kNegInf;
+      }
+      unsigned cs = __ballot_sync(0xffffffffu, lane < nst && mybm != kNegInf && mybm >= th);
+      while (cs) {
+        const int sc = __ffs(cs) - 1;
+        cs &= cs - 1;
+        list_block<DT>(p, d.rp, is_t, s0 + sc, warp, th, row, R);
+      }
+    }
     // ---- hand the piece's per-warp results to the epilogue warp ----
     float M, MC, Shi, Slo;
     warp_softmax_merge(a.m, a.mc, a.hi, a.lo, c, M, MC, Shi, Slo);
     if (lane == 0) {
-      R.wmax[warp] = wmax;
       R.m[warp] = M;
       R.hi[warp] = Shi;
       R.lo[warp] = Slo;
