@@ -82,13 +82,14 @@ void stream_chunking(int64_t NR, int V, int esize, int& nch, int& clen) {
 }
 
 // Chunks per group of the draws: enough for about one per CTA when groups
-// are few, each at least one stage.
+// are few, and at most about 16 stages each (a draw chunk occupies its CTA's
+// ring while rows wait), each at least one stage.
 int draw_chunks_per_group(int groups, int V, int esize) {
   const int64_t grid0 = stream_grid0();
   const int nsub = (V + kUnitB - 1) / kUnitB;
   const int ups = fused_units_per_stage(esize);
   const int stages = (nsub + ups - 1) / ups;
-  int64_t cpg = (grid0 + groups - 1) / groups;
+  int64_t cpg = std::max<int64_t>((grid0 + groups - 1) / groups, (stages + 15) / 16);
   cpg = std::max<int64_t>(1, std::min<int64_t>(cpg, stages));
   const int cu = (int)((nsub + cpg - 1) / cpg);
   return (nsub + cu - 1) / cu;

@@ -179,7 +179,7 @@ __device__ int scan_range(const CdfParams& p, const GroupParams& gp, const char*
 
 // Full two-pass draw over the whole row by one warp (degenerate residual).
 template <int DT>
-__device__ int full_row_draw(const CdfParams& p, const GroupParams& gp, const char* rt,
+__device__ __noinline__ int full_row_draw(const CdfParams& p, const GroupParams& gp, const char* rt,
                              const char* rd, double* Zout) {
   const int lane = threadIdx.x & 31;
   double loc = 0.0;
@@ -342,7 +342,7 @@ __device__ __forceinline__ void write_guesses(const CdfParams& p, int64_t g, con
 // Sums and prefixes are double-float pairs (see DF); a row whose weights
 // vanish in rounding falls back to the fp64 two-pass draw.
 template <int DT>
-__device__ void group_draw(const CdfParams& p, int64_t g) {
+__device__ __noinline__ void group_draw(const CdfParams& p, int64_t g) {
   constexpr int R = 16;  // unit sums per lane per round
   const int lane = threadIdx.x & 31;
   if (!SSD_CHK(g < p.groups, p.dbg, 20, g, p.groups)) return;
@@ -493,15 +493,17 @@ __device__ void group_draw(const CdfParams& p, int64_t g) {
   if (p.out_guess) write_guesses(p, g, p.rowres + g * p.rpg + p.nt, t);
 }
 
-// Sum of the draw weights of one whole unit whose elements sit 16-byte
-// aligned in shared memory (vectorised fast path of one warp), specialised
-// per kind of draw.
-template <int DT, int KIND, bool HAS_S>
+// Sum of the draw weights of one unit (SPLIT: of half h of it) whose
+// elements sit 16-byte aligned in shared memory (vectorised fast path of one
+// warp), specialised per kind of draw.
+template <int DT, int KIND, bool HAS_S, bool SPLIT>
 __device__ __forceinline__ float unit_sum_k(const CdfParams& p, const GroupParams& gp,
-                                            const Half& ht, const Half& hd, int ue0) {
+                                            const Half& ht, const Half& hd, int ue0, int h) {
   constexpr int VEC = Elem<DT>::kVec;
-  constexpr int NV = kUnitB / VEC / 32;
+  constexpr int NV = kUnitB / VEC / 32 / (SPLIT ? 2 : 1);
+  static_assert(NV >= 1, "a half unit is at least one vector per lane");
   const int lane = threadIdx.x & 31;
+  if (SPLIT) ue0 += h * (kUnitB / 2);
   const uint4* st4 = reinterpret_cast<const uint4*>(ht.sm + (ue0 - ht.ei0) * Elem<DT>::kSize);
   const uint4* sd4 = reinterpret_cast<const uint4*>(hd.sm + (ue0 - hd.ei0) * Elem<DT>::kSize);
   uint4 rt[NV], rd[NV];
@@ -527,18 +529,18 @@ __device__ __forceinline__ float unit_sum_k(const CdfParams& p, const GroupParam
   return s;
 }
 
-template <int DT>
+template <int DT, bool SPLIT>
 __device__ __forceinline__ float unit_sum_fast(const CdfParams& p, const GroupParams& gp,
-                                               const Half& ht, const Half& hd, int ue0) {
+                                               const Half& ht, const Half& hd, int ue0, int h) {
   const bool has_s = gp.theta != INFINITY;
   switch (kind_of(gp)) {
-    case kTarget: return unit_sum_k<DT, kTarget, false>(p, gp, ht, hd, ue0);
+    case kTarget: return unit_sum_k<DT, kTarget, false, SPLIT>(p, gp, ht, hd, ue0, h);
     case kSaguaro:
-      return has_s ? unit_sum_k<DT, kSaguaro, true>(p, gp, ht, hd, ue0)
-                   : unit_sum_k<DT, kSaguaro, false>(p, gp, ht, hd, ue0);
+      return has_s ? unit_sum_k<DT, kSaguaro, true, SPLIT>(p, gp, ht, hd, ue0, h)
+                   : unit_sum_k<DT, kSaguaro, false, SPLIT>(p, gp, ht, hd, ue0, h);
     default:
-      return has_s ? unit_sum_k<DT, kResidual, true>(p, gp, ht, hd, ue0)
-                   : unit_sum_k<DT, kResidual, false>(p, gp, ht, hd, ue0);
+      return has_s ? unit_sum_k<DT, kResidual, true, SPLIT>(p, gp, ht, hd, ue0, h)
+                   : unit_sum_k<DT, kResidual, false, SPLIT>(p, gp, ht, hd, ue0, h);
   }
 }
 
@@ -608,16 +610,23 @@ __device__ __forceinline__ void cdf_issue_stage(const CdfParams& p, const char* 
 
 // The weight sums of units [u, un) of group g, staged by cdf_issue_stage at
 // `stage`: consumer warp `warp` takes units u + warp, u + warp + 16, ...,
-// and its lane 0 stores each sum.  Units whose elements are not all in
-// shared memory, 16-byte aligned (row ends, unaligned rows), read the missing
-// ones from global memory.
+// and its lane 0 stores each sum.  A stage of at most half as many units as
+// consumer warps (fp32 rows read together) gives each unit two warps, one
+// per half: their sums meet in `half` (shared memory, [kConsumerWarps]) and
+// the first half's warp adds them, in that order.  Units whose elements are
+// not all in shared memory, 16-byte aligned (row ends, unaligned rows), read
+// the missing ones from global memory.  All consumer warps call it.
 template <int DT>
 __device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
                                                   const GroupParams& gp, const char* rt,
                                                   const char* rd, int u, int un,
                                                   const unsigned char* stage,
-                                                  const DrawLayout& lay, int warp) {
-  if (u + warp >= un || no_draw(gp)) return;
+                                                  const DrawLayout& lay, int warp,
+                                                  float* half) {
+  if (no_draw(gp)) return;
+  constexpr int kPair = kConsumerWarps / 2;
+  const bool split = 2 * (un - u) <= kConsumerWarps;  // the same in every consumer warp
+  if (!split && u + warp >= un) return;
   const int e0 = u * kUnitB;
   const int e1 = min(p.V, un * kUnitB);
   Half ht, hd;
@@ -640,26 +649,49 @@ __device__ __forceinline__ void cdf_consume_stage(const CdfParams& p, int64_t g,
     }
   }
   const int lane = threadIdx.x & 31;
-  for (int uu = u + warp; uu < un; uu += kConsumerWarps) {
-    const int ue0 = uu * kUnitB;
-    const int ue1 = min(ue0 + kUnitB, p.V);
-    constexpr int VEC = Elem<DT>::kVec;
+  constexpr int VEC = Elem<DT>::kVec;
+  auto fast_unit = [&](int ue0, int ue1) {
     bool fast = ue1 - ue0 == kUnitB;
     if (gp.use_t) fast &= ue0 >= ht.ei0 && ue1 <= ht.ei1 && (ue0 - ht.ei0) % VEC == 0;
     if (gp.use_d) fast &= ue0 >= hd.ei0 && ue1 <= hd.ei1 && (ue0 - hd.ei0) % VEC == 0;
+    return fast;
+  };
+  // the elements [y0, y1) one by one (lane-strided)
+  auto slow_sum = [&](int y0, int y1) {
     float s = 0.f;
-    if (fast) {
-      s = unit_sum_fast<DT>(p, gp, ht, hd, ue0);
-    } else {
-      for (int m = 0; m < kUnitB / 32; ++m) {
-        const int y = ue0 + lane + 32 * m;
-        if (y < ue1) {
-          const float zt = gp.use_t ? fetch<DT>(ht, y, p, true, lay.cap) : 0.f;
-          const float zd = gp.use_d ? fetch<DT>(hd, y, p, false, lay.cap) : 0.f;
-          s += weight(gp, gp.c, y, zt, zd);
-        }
+    for (int y = y0 + lane; y < y1; y += 32) {
+      const float zt = gp.use_t ? fetch<DT>(ht, y, p, true, lay.cap) : 0.f;
+      const float zd = gp.use_d ? fetch<DT>(hd, y, p, false, lay.cap) : 0.f;
+      s += weight(gp, gp.c, y, zt, zd);
+    }
+    return s;
+  };
+  if (split) {
+    const int uu = u + warp % kPair, h = warp / kPair;
+    float s = 0.f;
+    if (uu < un) {
+      const int ue0 = uu * kUnitB;
+      const int ue1 = min(ue0 + kUnitB, p.V);
+      if (fast_unit(ue0, ue1)) {
+        s = unit_sum_fast<DT, true>(p, gp, ht, hd, ue0, h);
+      } else {
+        const int m = ue0 + kUnitB / 2;
+        s = h == 0 ? slow_sum(ue0, min(m, ue1)) : slow_sum(m, ue1);
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) half[warp] = s;
+    consumer_sync();
+    if (h == 0 && uu < un && lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
+      p.subsum[g * p.nsub + uu] = half[warp] + half[warp + kPair];
+    return;
+  }
+  for (int uu = u + warp; uu < un; uu += kConsumerWarps) {
+    const int ue0 = uu * kUnitB;
+    const int ue1 = min(ue0 + kUnitB, p.V);
+    float s = fast_unit(ue0, ue1) ? unit_sum_fast<DT, false>(p, gp, ht, hd, ue0, 0)
+                                  : slow_sum(ue0, ue1);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0 && SSD_CHK(uu < p.nsub && g < p.groups, p.dbg, 23, uu, g))
@@ -699,7 +731,7 @@ __device__ __forceinline__ void cdf_chunk_done(const CdfParams& p, int64_t g, in
 // Sums and prefixes are double-float pairs, as in group_draw.  One warp;
 // rr (Saguaro: the row's top list, null for p_K) gives S and the guesses.
 template <int DT>
-__device__ void direct_draw(const CdfParams& p, const float2* bs, int nblk, const GroupParams& gp,
+__device__ __noinline__ void direct_draw(const CdfParams& p, const float2* bs, int nblk, const GroupParams& gp,
                             int64_t g, const RowResult* rr, int F) {
   constexpr int R = 16;  // block sums per lane per round
   constexpr int ES = Elem<DT>::kSize;

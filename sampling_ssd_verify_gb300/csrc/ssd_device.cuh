@@ -123,12 +123,18 @@ __device__ __forceinline__ bool flag_wait(const int* f, volatile int* s_err, int
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
-// dst, src and bytes must be multiples of 16.
+// dst, src and bytes must be multiples of 16.  The streamed rows are read
+// once (or re-read soon after), so their L2 lines are marked evict-first:
+// they displace one another rather than the kernel's code, its counters and
+// its per-row results, which the rarer paths (draws, decisions) would
+// otherwise fetch again from HBM.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
+      "{.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], pol;}" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }

@@ -521,7 +521,7 @@ __device__ __forceinline__ void list_block(const StreamParams& p, const char* rp
 // The chunk's top list: wm = lane w's warp maximum (lanes >= 16: -inf),
 // v[j] = the maximum of block lane + 32 j.
 template <int DT>
-__device__ void chunk_top(const StreamParams& p, int64_t row, int s0, float wm,
+__device__ __noinline__ void chunk_top(const StreamParams& p, int64_t row, int s0, float wm,
                           const float (&v)[16], WarpList& wl) {
   const int lane = threadIdx.x & 31;
   // theta: the R-th largest warp maximum (-inf when fewer than R warps saw data)
@@ -659,7 +659,8 @@ __device__ __forceinline__ void mark_decided(const StreamParams& p) {
 // write k, then either the greedy outputs, a direct draw of p_K from the
 // streaming pass's block sums, or the draw's chunks to the ticket queue.
 template <int DT>
-__device__ void decide(const StreamParams& p, const CdfParams& cq, int64_t g, int k, float cf) {
+__device__ __noinline__ void decide(const StreamParams& p, const CdfParams& cq, int64_t g, int k,
+                                   float cf) {
   const int lane = threadIdx.x & 31;
   const int K = p.K;
   if (!SSD_CHK(g < p.B && k >= 0 && k <= K, p.dbg, 8, g, k)) return;
@@ -729,11 +730,12 @@ __device__ void decide(const StreamParams& p, const CdfParams& cq, int64_t g, in
   }
   if (k == K && p.bsum != nullptr) {
     // all accepted: the bonus is drawn from p_K with the block sums that the
-    // streaming pass stored for target row K
+    // streaming pass stored for target row K (no ticket: count it as decided
+    // first, so that idle producers need not wait for the draw)
+    if (lane == 0) mark_decided(p);
     __syncwarp();
     gp = load_gp(p.gparams + g);
     direct_draw<DT>(cq, p.bsum + g * p.nblk, p.nblk, gp, g, nullptr, 0);
-    if (lane == 0) mark_decided(p);
     return;
   }
   if (lane == 0) {
@@ -745,7 +747,7 @@ __device__ void decide(const StreamParams& p, const CdfParams& cq, int64_t g, in
 // Saguaro continuation draw of branch row g: the parameters of q', then the
 // draw from the block sums (aligned rows) or the draw's chunks queued.
 template <int DT>
-__device__ void saguaro_finish(const StreamParams& p, const CdfParams& cq, int64_t g,
+__device__ __noinline__ void saguaro_finish(const StreamParams& p, const CdfParams& cq, int64_t g,
                                const RowResult& rr, float cf) {
   const int lane = threadIdx.x & 31;
   const int F = saguaro_F(p, g);
@@ -785,10 +787,10 @@ __device__ void saguaro_finish(const StreamParams& p, const CdfParams& cq, int64
     p.gparams[g] = gp;
   }
   if (p.bsum != nullptr) {
+    if (lane == 0) mark_decided(p);
     __syncwarp();
     const GroupParams gp = load_gp(p.gparams + g);
     direct_draw<DT>(cq, p.bsum + g * p.nblk, p.nblk, gp, g, p.rowres + g, F);
-    if (lane == 0) mark_decided(p);
     return;
   }
   if (lane == 0) {
@@ -803,7 +805,7 @@ __device__ void saguaro_finish(const StreamParams& p, const CdfParams& cq, int64
 // xs / zxs: the row's draft token and its logit when the streaming pass
 // captured them (have_x), else they are read here.
 template <int DT>
-__device__ void finalize_row(const StreamParams& p, const CdfParams& cq, int64_t row, float c,
+__device__ __noinline__ void finalize_row(const StreamParams& p, const CdfParams& cq, int64_t row, float c,
                              float M, float MC, float Shi, float Slo, const WarpList& wl,
                              int need, bool have_x, int xs, float zxs, bool* cleared,
                              volatile int* s_err) {
@@ -950,6 +952,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   // row's draft-token logit out of the staged data, so the epilogue needs no
   // global gather.
   __shared__ int s_tok[kTokCache];
+  // half-unit sums of a draw stage (two buffers: consecutive stages alternate,
+  // kStagesA being even)
+  static_assert(kStagesA % 2 == 0, "ring slots alternate in parity");
+  __shared__ float s_half[2 * kConsumerWarps];
   const bool tok_smem = p.tokens != nullptr && (int64_t)p.B * p.tokK <= kTokCache;
 
   const int tid = threadIdx.x;
@@ -980,48 +986,70 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       // the first round of row chunks is static (chunk = CTA): a CTA's first
       // copy does not wait behind every CTA's atomic on the counter
       unsigned long long next = blockIdx.x;
-      // Draw tickets.  The queue's head and tail (qh, qt) are loaded one
-      // piece before they are read, and a ticket claimed at one piece
-      // boundary has its entry read at the next, so the producer waits on a
-      // global round trip only when it has a ticket to look at.
+      // Draw tickets.  At a piece boundary a producer that saw queued draws
+      // nobody has taken claims a ticket (the first producer to reach a
+      // boundary takes a new draw); a claimed ticket whose draw is not yet
+      // published is held and read again at the next boundary.  The queue
+      // counters and the held entry are loaded before the wait for a free
+      // ring slot and read after it.
       long long ticket = -1;
-      unsigned qh = 0, qt = 0;
+      bool ticket_ok = draws;  // tickets may still carry draws
+      bool slot_held = false;  // the ring slot of stage n is free
       for (int piece = 0;; ++piece) {
         long long c = -1;
-        // 1. a draw chunk whose ticket is ready goes first: its rows were
-        //    just streamed and are still in L2
-        if (ticket >= (long long)maxT) ticket = -1;
+        int e = 0;
+        unsigned qh = 0, qt = 0;
         if (ticket >= 0) {
-          const int e = flag_acquire(p.dq_entry + ticket);
-          if (e > 0) {
-            c = nS + (e - 1);
-            ticket = -1;
+          e = (int)ld_relaxed_u32(reinterpret_cast<const unsigned*>(p.dq_entry + ticket));
+        } else if (ticket_ok) {
+          qh = ld_relaxed_u32(p.dq_head);
+          qt = ld_relaxed_u32(p.dq_tail);
+        }
+        // the ring slot of the piece's first stage
+        if (n >= kStagesA) mbar_wait(empty + n % kStagesA, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+        slot_held = true;
+        if (ticket < 0 && ticket_ok && qh < qt) {
+          const unsigned t = atomicAdd(p.dq_head, 1u);
+          if (t < maxT) {
+            ticket = t;
+            e = (int)ld_relaxed_u32(reinterpret_cast<const unsigned*>(p.dq_entry + t));
+          } else {
+            ticket_ok = false;
           }
+        }
+        // 1. a draw chunk whose ticket is ready goes first
+        if (e > 0) {
+          __threadfence();  // acquire: the group's parameters after its entry
+          c = nS + (e - 1);
+          ticket = -1;
         }
         // 2. the next row chunk (its id was fetched one piece ago)
         if (c < 0 && next < (unsigned long long)nS) {
           c = (long long)next;
           next = gridDim.x + atomicAdd(p.chunk_ctr, 1ull);
         }
-        // 3. nothing left to stream: wait for the draws still to come
+        // 3. nothing left to stream: wait for the draws still to come.  The
+        //    producer leaves once every group is decided (no more draws can
+        //    be queued) and its ticket has no draw.
         if (c < 0 && draws) {
           const unsigned long long t0 = global_ns();
           while (!s_err) {
-            if (ticket < 0) {
+            if (ticket < 0 && ticket_ok) {
               const unsigned t = atomicAdd(p.dq_head, 1u);
-              if (t >= maxT) break;
-              ticket = t;
+              if (t < maxT) ticket = t;
+              else ticket_ok = false;
             }
-            if (ticket >= (long long)maxT) break;
-            const int ev = flag_acquire(p.dq_entry + ticket);
-            if (ev > 0) {
-              c = nS + (ev - 1);
-              ticket = -1;
-              break;
+            if (ticket >= 0) {
+              const int ev = flag_acquire(p.dq_entry + ticket);
+              if (ev > 0) {
+                c = nS + (ev - 1);
+                ticket = -1;
+                break;
+              }
             }
             if (flag_acquire(p.decided) >= cq.groups &&
-                (unsigned)ticket >= ld_acquire_u32(p.dq_tail))
-              break;  // every group is decided and this ticket has no draw
+                (ticket < 0 || (unsigned)ticket >= ld_acquire_u32(p.dq_tail)))
+              break;
             __nanosleep(128);
             if (global_ns() - t0 > kWaitLimitNs) {
               s_err = 1;
@@ -1029,13 +1057,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
               break;
             }
           }
-        }
-        // for the next boundary: a claim and relaxed loads whose results are
-        // read only there
-        if (draws && c >= 0) {
-          if (ticket < 0 && qh < qt) ticket = atomicAdd(p.dq_head, 1u);
-          qh = ld_relaxed_u32(p.dq_head);
-          qt = ld_relaxed_u32(p.dq_tail);
         }
         PieceDesc& d = s_pq[piece % kPieceQueue];
         if (c >= nS) {
@@ -1053,10 +1074,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
         d.chunk = c;
         if (c < 0) {
-          // end marker: one stage without data
-          const int slot = n % kStagesA;
-          if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
-          mbar_arrive(full + slot);
+          // end marker: one stage without data (its slot is held)
+          mbar_arrive(full + n % kStagesA);
           ++n;
           break;
         }
@@ -1068,7 +1087,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           for (int u = d.u0, un = 0; u < d.u1; u = un) {
             un = min(u + lay.ups, d.u1);
             const int slot = n % kStagesA;
-            if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+            if (!slot_held && n >= kStagesA)
+              mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+            slot_held = false;
             cdf_issue_stage<DT>(cq, rt, rd, u, un, ring + slot * kStageBytes, lay, full + slot,
                                 &s_err);
             ++n;
@@ -1097,7 +1118,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           un = min(u + ups, pu1);
           const Stage st = stage_of<DT>(rp, p.V, (int)((u - row * p.upr) / ups));
           const int slot = n % kStagesA;
-          if (n >= kStagesA) mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+          if (!slot_held && n >= kStagesA)
+            mbar_wait(empty + slot, ((n / kStagesA) - 1) & 1, &s_err, p.status);
+          slot_held = false;
           StageDesc& sd = s_sd[slot];
           sd.nvec = (int)((st.a1 - st.a0) >> 4);
           sd.ei0 = st.e0 + (int)((st.a0 - st.b0) / Elem<DT>::kSize);
@@ -1344,7 +1367,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       for (int u = u0, un = 0; u < u1; u = un) {
         un = min(u + lay.ups, u1);
         if (u != u0) mbar_wait(full + slot, phase, &s_err, p.status);
-        cdf_consume_stage<DT>(cq, g, gp, rt, rd, u, un, ring + slot * kStageBytes, lay, warp);
+        cdf_consume_stage<DT>(cq, g, gp, rt, rd, u, un, ring + slot * kStageBytes, lay, warp,
+                              s_half + (slot & 1) * kConsumerWarps);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + slot);
         if (++slot == kStagesA) {
