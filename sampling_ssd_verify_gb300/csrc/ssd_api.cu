@@ -180,9 +180,12 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   }
   p.d_lo = static_cast<const char*>(draft->ptr);
   p.d_hi = p.d_lo + ((int64_t)(groups * Kq - 1) * draft->row_stride + V) * es;
-  p.dbg = reinterpret_cast<unsigned long long*>(ws + L.dbg_off);
+  // the bounds-check record of SSD_CHECKS builds: the caller's last 256
+  // bytes (8-byte aligned), whatever layout this launch uses
+  const size_t dbg_at = (ws_bytes - 256) & ~(size_t)7;
+  p.dbg = reinterpret_cast<unsigned long long*>(ws + dbg_at);
 #ifdef SSD_CHECKS
-  e = cudaMemsetAsync(ws + L.dbg_off, 0, 256, stream);
+  e = cudaMemsetAsync(ws + dbg_at, 0, 256, stream);
   if (e != cudaSuccess) return cuda_status(e);
 #endif
   CdfParams& q = cm.cp;
