@@ -1,7 +1,9 @@
 // ssd_api.cu -- the C-ABI entry points: argument validation, workspace
 // layout, launch configuration.  All arithmetic runs in the kernels of
-// ssd_stream.cu (the streaming pass with the draws of ssd_cdf_dev.cuh) and
-// ssd_cache.cu; the one host computation is the fan-out helper.
+// ssd_stream_kernel.cuh (the streaming pass with the draws of
+// ssd_cdf_dev.cuh, instantiated by ssd_stream_bf16.cu / ssd_stream_f32.cu),
+// ssd_tree.cu and ssd_cache.cu; the one host computation is the fan-out
+// helper.
 //
 // Sources: [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈";
 // [SD-7.3] "7.3 Speculative Decoding：投机采样加速".

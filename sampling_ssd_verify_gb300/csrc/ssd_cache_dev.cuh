@@ -1,6 +1,6 @@
 // ssd_cache_dev.cuh -- device code of the outcome cache, shared by the cache
 // kernels (ssd_cache.cu) and the verify kernel that builds and probes a
-// round's cache in the same launch (ssd_stream.cu).
+// round's cache in the same launch (ssd_stream_kernel.cuh).
 //
 // [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈",
 // §"SSD 的核心思想": the outcome of a sequence is (k accepted, bonus t); the

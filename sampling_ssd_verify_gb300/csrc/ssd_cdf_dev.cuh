@@ -1,5 +1,5 @@
 // ssd_cdf_dev.cuh -- device code of the inverse-CDF draw, which the
-// streaming kernel (ssd_stream.cu) runs after the rows in the same launch.
+// streaming kernel (ssd_stream_kernel.cuh) runs after the rows in the same launch.
 //
 // The bonus weight of a verified sequence is w(y) = (p_k(y) - q'_k(y))^+
 // after a rejection at k < K and w(y) = p_K(y) when every draft was accepted

@@ -294,15 +294,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Order-preserving map of a (non-NaN) float to uint32 and back.
-__device__ __forceinline__ uint32_t ord_float(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float unord_float(uint32_t u) {
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
-}
-
 // Error-free sum of two floats (Knuth): a + b = s + e exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = a + b;
@@ -355,93 +346,6 @@ __device__ __forceinline__ double uniform24(uint64_t seed, uint32_t c0, uint32_t
 // ---- candidate lists (top-F by raw logit, ties to the lower index) -----------------------
 __device__ __forceinline__ bool cand_before(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);
-}
-
-// Insert (x, ix) into a descending list of TOPK entries.  Elements of one
-// thread arrive in increasing index order, so a strict comparison keeps the
-// lower index first among equal logits.
-template <int TOPK>
-__device__ __forceinline__ void topk_insert(float (&tv)[TOPK > 0 ? TOPK : 1],
-                                            int (&ti)[TOPK > 0 ? TOPK : 1], float x, int ix) {
-#pragma unroll
-  for (int k = TOPK - 1; k >= 0; --k) {
-    const float up = (k > 0) ? tv[k > 0 ? k - 1 : 0] : __int_as_float(0x7f800000);
-    const int upi = (k > 0) ? ti[k > 0 ? k - 1 : 0] : 0;
-    if (x > tv[k]) {
-      if (x > up) {
-        tv[k] = up;
-        ti[k] = upi;
-      } else {
-        tv[k] = x;
-        ti[k] = ix;
-      }
-    }
-  }
-}
-
-// Insert with the full (value desc, index asc) order, for merges of lists
-// whose elements do not arrive in index order.
-template <int TOPK>
-__device__ __forceinline__ void topk_insert_ordered(float (&tv)[TOPK > 0 ? TOPK : 1],
-                                                    int (&ti)[TOPK > 0 ? TOPK : 1], float x,
-                                                    int ix) {
-#pragma unroll
-  for (int k = TOPK - 1; k >= 0; --k) {
-    const bool above_k = cand_before(x, ix, tv[k], ti[k]);
-    const bool above_up = (k == 0) ? false : cand_before(x, ix, tv[k > 0 ? k - 1 : 0],
-                                                         ti[k > 0 ? k - 1 : 0]);
-    if (above_k) {
-      if (above_up) {
-        tv[k] = tv[k > 0 ? k - 1 : 0];
-        ti[k] = ti[k > 0 ? k - 1 : 0];
-      } else {
-        tv[k] = x;
-        ti[k] = ix;
-      }
-    }
-  }
-}
-
-// Warp-wide merge of per-lane sorted top lists (value desc, index asc; -inf
-// padding): every lane ends with the first `rounds` (<= TOPK) entries of the
-// merged order, the rest padding.  One round takes the warp maximum of the
-// lanes' heads with two integer reductions (ordered value, then index; an
-// element lives in one list only, so ties between lanes are padding, broken
-// by the lowest lane) and pops it from the winning lane.
-template <int TOPK>
-__device__ __forceinline__ void warp_topk_merge(float (&tv)[TOPK > 0 ? TOPK : 1],
-                                                int (&ti)[TOPK > 0 ? TOPK : 1], int rounds) {
-  const int lane = threadIdx.x & 31;
-  float ov[TOPK > 0 ? TOPK : 1];
-  int oi[TOPK > 0 ? TOPK : 1];
-#pragma unroll
-  for (int r = 0; r < TOPK; ++r) {
-    ov[r] = __int_as_float(0xff800000);
-    oi[r] = 0x7fffffff;
-    if (r < rounds) {  // warp-uniform
-      const uint32_t key = ord_float(tv[0]);
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const bool head = key == kmax;
-      const uint32_t imin = __reduce_min_sync(0xffffffffu, head ? (uint32_t)ti[0] : 0xffffffffu);
-      const unsigned win = __ballot_sync(0xffffffffu, head && (uint32_t)ti[0] == imin);
-      ov[r] = unord_float(kmax);
-      oi[r] = (int)imin;
-      if (lane == __ffs(win) - 1) {  // pop the head of the winning lane's list
-#pragma unroll
-        for (int k = 0; k < TOPK - 1; ++k) {
-          tv[k] = tv[k + 1];
-          ti[k] = ti[k + 1];
-        }
-        tv[TOPK - 1] = __int_as_float(0xff800000);
-        ti[TOPK - 1] = 0x7fffffff;
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < TOPK; ++r) {
-    tv[r] = ov[r];
-    ti[r] = oi[r];
-  }
 }
 
 // Warp-wide merge of (max, compensated sum) partials.  Each lane holds

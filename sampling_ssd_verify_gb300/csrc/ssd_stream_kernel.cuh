@@ -2,27 +2,29 @@
 // rows and the draws that follow it, in one persistent launch (instantiated
 // per element type by ssd_stream_bf16.cu and ssd_stream_f32.cu).
 //
-// Work: one persistent CTA per SM.  Its producer warp takes row chunks from
-// a global counter (the first round static: chunk = CTA) and draw chunks
-// from a ticket queue, and streams them through a ring of kStagesA 32 KB
-// shared-memory stages with 1-D bulk copies (cp.async.bulk, mbarrier
-// transaction counts).  Sixteen consumer warps reduce each stage; each owns
-// one block of 128 consecutive 16-byte vectors of the stage.  Two epilogue
-// warps take alternate pieces and do every global-memory epilogue step, so
-// the consumers never wait for one.
+// Work: one persistent CTA per SM (a cooperative launch: CTAs wait on work
+// other CTAs do).  Its producer warp takes row chunks from a global counter
+// (the first round static: chunk = CTA) and draw chunks from a ticket queue,
+// and streams them through a ring of kStagesA 32 KB shared-memory stages with
+// 1-D bulk copies (cp.async.bulk, mbarrier transaction counts, L2
+// evict-first).  Sixteen consumer warps reduce each stage; each owns one
+// block of 128 consecutive 16-byte vectors of the stage.  Three epilogue
+// warps take pieces in turn (piece p to warp p mod 3) and do every
+// global-memory epilogue step, so the consumers never wait for one.
 //
 // A row chunk gives, per row ([SD-7.3] §7.3.2: the target and draft
 // distributions of every position):
 //   * the online-softmax normaliser: max raw logit m and
 //     s = sum_y 2^(z_y * c - fl(m*c)), c = log2(e)/T, compensated fp32 sums
 //     per thread, merged per warp and per row;
+//   * the logit of the row's draft token, picked out of the staged data;
 //   * the top-(F_j+1) raw logits (ties to the lower index) of the draft rows
 //     ([SSD-note] §"怎么猜奖励 token", §"Saguaro 优化二：Saguaro 采样"): the
-//     consumers only record each block's maximum; the epilogue takes theta =
-//     the R-th largest block maximum (at least R logits reach it, so no
-//     logit below it is in the top R), reads the blocks whose maximum
-//     reaches theta again (from L2, just streamed) and keeps their logits
-//     >= theta in a warp-wide sorted list;
+//     consumers record each block's and each warp's maximum; at the end of
+//     the piece theta = the R-th largest warp maximum (R warps hold a logit
+//     >= theta, so no logit below it is in the top R), each warp reads its
+//     blocks whose maximum reaches theta again and lists their logits
+//     >= theta; the epilogue keeps the best R in a warp-wide sorted list;
 //   * for rows whose draw weight has one term (Saguaro rows, target row K),
 //     each block's sum, so that the draw needs no second pass.
 //
@@ -31,10 +33,10 @@
 // i are both final the accept test u_i < p_i(x_i)/q'_i(x_i) runs at once
 // ([SD-7.3] §7.3.3; [SD-blog] §"三、接受概率为什么是对的").  A sequence is
 // decided when its first rejection k has every earlier position accepted (or
-// all K are accepted and position K is done); its bonus draw then runs while
-// later positions are still streaming, and reads the two rows it needs from
-// L2.  Draws of two-term weights (p - q')^+ are cut into chunks pushed to a
-// ticket queue; producers take a ready ticket before their next row chunk.
+// all K are accepted and target row K is done).  The all-accepted bonus is
+// drawn at once from target row K's block sums; a residual (p - q')^+ draw
+// is cut into chunks pushed to a ticket queue, which producers serve before
+// their next row chunk, while later positions are still streaming.
 //
 // Sources: [SSD-note] "论文阅读：Speculative Speculative Decoding — 消除推测解码的最后一个顺序瓶颈";
 // [SD-7.3] "7.3 Speculative Decoding：投机采样加速";
