@@ -169,9 +169,9 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.dq_entry = cnt + L.o_dq;
   p.seq_state = reinterpret_cast<unsigned long long*>(ws + L.cnt_off) + L.o_state;
   p.chunk_ctr = w8;
-  p.dq_tail = reinterpret_cast<unsigned int*>(w8 + 3);
-  p.dq_head = reinterpret_cast<unsigned int*>(w8 + 4);
-  p.decided = reinterpret_cast<int*>(w8 + 5);
+  p.dq_tail = reinterpret_cast<unsigned int*>(w8 + 3 * kCtrStride);
+  p.dq_head = reinterpret_cast<unsigned int*>(w8 + 4 * kCtrStride);
+  p.decided = reinterpret_cast<int*>(w8 + 5 * kCtrStride);
   p.partials = reinterpret_cast<RowPartial*>(ws + L.part_off);
   p.rowres = reinterpret_cast<RowResult*>(ws + L.rowres_off);
   p.gparams = reinterpret_cast<GroupParams*>(ws + L.gp_off);
@@ -375,8 +375,8 @@ ssd_status verify_impl(const ssd_logits* target, const ssd_logits* draft, int B,
     p.rc.cap = cache_cap;
     p.rc.branch = ra->out_branch;
     p.rc.all_hit = ra->all_hit;
-    p.rc.cnt = w8 + 1;
-    p.rc.cleared = reinterpret_cast<int*>(w8 + 2);
+    p.rc.cnt = w8 + 1 * kCtrStride;
+    p.rc.cleared = reinterpret_cast<int*>(w8 + 2 * kCtrStride);
     cm.cp.rc = p.rc;
   }
   p.need_top = need_top ? 1 : 0;

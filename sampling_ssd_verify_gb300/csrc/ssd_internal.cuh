@@ -253,6 +253,9 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// spacing of the 8-byte counters (in 8-byte words): one 128-byte line each
+constexpr int kCtrStride = 16;
+
 // groups of rpg rows (nt target rows, K positions), V elements per row of
 // esize bytes, nch chunks per row, cpg draw chunks per group; bsum: room for
 // the one-row draws' block sums (one row per group).
@@ -279,8 +282,10 @@ inline WsLayout ws_layout(int groups, int rpg, int K, int V, int esize, int nch,
   const size_t nint = L.o_dq + (size_t)groups * cpg;
   L.cnt_off = 0;
   L.o_state = ((nint * sizeof(int) + 7) & ~(size_t)7) / 8;  // in 8-byte words
-  L.ctr_off = (L.o_state + (size_t)groups) * 8;
-  L.cnt_bytes = align256(L.ctr_off + 6 * sizeof(unsigned long long));
+  // each 8-byte counter on its own 128-byte line: CTAs poll some of them
+  // while others are incremented
+  L.ctr_off = ((L.o_state + (size_t)groups) * 8 + 127) & ~(size_t)127;
+  L.cnt_bytes = align256(L.ctr_off + 6 * kCtrStride * sizeof(unsigned long long));
   L.part_off = L.cnt_bytes;
   const size_t slots = nch > 1 ? (size_t)L.NR * nch : 1;
   L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));

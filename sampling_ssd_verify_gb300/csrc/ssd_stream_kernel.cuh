@@ -1041,18 +1041,25 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
               if (t < maxT) ticket = t;
               else ticket_ok = false;
             }
-            if (ticket >= 0) {
-              const int ev = flag_acquire(p.dq_entry + ticket);
-              if (ev > 0) {
-                c = nS + (ev - 1);
-                ticket = -1;
-                break;
-              }
-            }
-            if (flag_acquire(p.decided) >= cq.groups &&
-                (ticket < 0 || (unsigned)ticket >= ld_acquire_u32(p.dq_tail)))
+            // one round trip per poll: the words are loaded together (relaxed)
+            const int ev = ticket >= 0 ? (int)ld_relaxed_u32(
+                                             reinterpret_cast<const unsigned*>(p.dq_entry + ticket))
+                                       : 0;
+            const int dec = (int)ld_relaxed_u32(reinterpret_cast<const unsigned*>(p.decided));
+            if (ev > 0) {
+              __threadfence();  // acquire: the group's parameters after its entry
+              c = nS + (ev - 1);
+              ticket = -1;
               break;
-            __nanosleep(128);
+            }
+            // every group decided: the tail is final (each push precedes its
+            // group's decided count), read after an acquire fence
+            if (dec >= cq.groups) {
+              __threadfence();
+              if (ticket < 0 || (unsigned)ticket >= ld_acquire_u32(p.dq_tail)) break;
+            }
+            // a producer without a ticket only waits for the end
+            __nanosleep(ticket >= 0 ? 128 : 1024);
             if (global_ns() - t0 > kWaitLimitNs) {
               s_err = 1;
               if (p.status) atomicOr(p.status, SSD_DEV_TIMEOUT);
@@ -1312,11 +1319,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       WarpList rl;
       rl.reset(need > 0 ? need : 1);
       if (need > 0) {
-        for (int cc = 0; cc < p.nch; ++cc) {
-          const RowPartial* pp = p.partials + (row * p.nch + cc);
-          const float x = lane < need ? __ldcg(&pp->tv[lane]) : kNegInf;
-          const int ix = lane < need ? __ldcg(&pp->ti[lane]) : 0x7fffffff;
-          rl.offer(x, ix, x != kNegInf);
+        // the chunks' lists, eight chunks' loads in flight at a time
+        constexpr int kB = 8;
+        for (int c0 = 0; c0 < p.nch; c0 += kB) {
+          float xs[kB];
+          int is[kB];
+#pragma unroll
+          for (int q = 0; q < kB; ++q) {
+            const bool ok = c0 + q < p.nch && lane < need;
+            const RowPartial* pp = p.partials + (row * p.nch + c0 + q);
+            xs[q] = ok ? __ldcg(&pp->tv[lane]) : kNegInf;
+            is[q] = ok ? __ldcg(&pp->ti[lane]) : 0x7fffffff;
+          }
+#pragma unroll
+          for (int q = 0; q < kB; ++q) rl.offer(xs[q], is[q], xs[q] != kNegInf);
         }
       }
       finalize_row<DT>(p, cq, row, c, M, MC, Shi, Slo, rl, need, x >= 0, x, zxm, &cleared,
