@@ -520,10 +520,44 @@ __device__ __forceinline__ float unit_sum_k(const CdfParams& p, const GroupParam
     if (KIND != kSaguaro) Elem<DT>::unpack(rt[m], zt);
     if (KIND != kTarget) Elem<DT>::unpack(rd[m], zd);
     float sv = 0.f;
+    if constexpr (KIND == kResidual) {
+      // (p - q')^+ with the two exponent arguments and the two scalings as
+      // packed f32x2 operations (the roundings of weight_k, element by
+      // element); the set S's larger scale only where a draft logit reaches
+      // theta (S holds the top F logits, theta the F-th)
+      bool inS_any = false;
+      if (HAS_S) {
+        float mx = zd[0];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e)
-      sv += weight_k<KIND, HAS_S>(gp, gp.c, ue0 + vi * VEC + e, KIND != kSaguaro ? zt[e] : 0.f,
-                                  KIND != kTarget ? zd[e] : 0.f);
+        for (int e = 1; e < VEC; ++e) mx = fmaxf(mx, zd[e]);
+        inS_any = mx >= gp.theta;
+      }
+      if (!inS_any) {
+        const unsigned long long cc = pack2(gp.c, gp.c), mm = pack2(-gp.mc_t, -gp.mc_d);
+        const unsigned long long sc = pack2(gp.inv_st, gp.scale_out);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          unsigned long long a, w;
+          asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(a) : "l"(pack2(zt[e], zd[e])), "l"(cc),
+              "l"(mm));
+          float at, ad;
+          unpack2(a, at, ad);
+          asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(w) : "l"(pack2(ex2(at), ex2(ad))), "l"(sc));
+          float pt, q;
+          unpack2(w, pt, q);
+          sv += fmaxf(pt - q, 0.f);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          sv += weight_k<KIND, HAS_S>(gp, gp.c, ue0 + vi * VEC + e, zt[e], zd[e]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+        sv += weight_k<KIND, HAS_S>(gp, gp.c, ue0 + vi * VEC + e, KIND != kSaguaro ? zt[e] : 0.f,
+                                    KIND != kTarget ? zd[e] : 0.f);
+    }
     s += sv;
   }
   return s;

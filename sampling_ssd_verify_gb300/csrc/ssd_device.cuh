@@ -151,6 +151,9 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* f) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_relaxed_s32(int* f, int v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_release_s32(int* f, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
@@ -285,6 +288,17 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Two floats as one 64-bit register pair (the operands of the packed f32x2
+// instructions) and back.
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
 }
 
 // max(a, b, c) in one instruction (three-operand max.f32 of sm_100+).

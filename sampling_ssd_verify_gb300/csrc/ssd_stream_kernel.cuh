@@ -147,16 +147,6 @@ __device__ __forceinline__ Stage stage_of(const char* rp, int V, int s) {
   return st;
 }
 
-// Two floats as one 64-bit register pair, for the packed f32x2 instructions.
-__device__ __forceinline__ unsigned long long pack2(float a, float b) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void unpack2(unsigned long long r, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-
 // Named barrier 2: the consumer warps wait (bar.sync) until the epilogue
 // warps have loaded the draft tokens into shared memory (bar.arrive).
 constexpr int kTokBarThreads = kConsumers + kEpilogueWarps * 32;
@@ -639,15 +629,17 @@ __device__ bool accept_test(const StreamParams& p, int64_t g, int i, float cf) {
   return u < pt / qp;
 }
 
-// Queue the draw chunks of group g (one lane): the tickets are reserved,
-// then each entry is published with a release store.
+// Queue the draw chunks of group g (one lane): one fence orders the group's
+// parameters before everything that follows, the tickets are reserved, and
+// the entries are written with plain (relaxed) stores, back to back; a
+// producer that reads an entry fences before it reads the parameters.
 __device__ __forceinline__ void push_draw(const StreamParams& p, const CdfParams& cq, int64_t g) {
   __threadfence();
   const unsigned base = atomicAdd(p.dq_tail, (unsigned)cq.cpg);
   for (int c = 0; c < cq.cpg; ++c) {
     const int64_t e = (int64_t)base + c;
     if (SSD_CHK(e < (int64_t)cq.groups * cq.cpg, p.dbg, 40, e, g))
-      st_release_s32(p.dq_entry + e, (int)(g * cq.cpg + c) + 1);
+      st_relaxed_s32(p.dq_entry + e, (int)(g * cq.cpg + c) + 1);
   }
 }
 
@@ -709,8 +701,13 @@ __device__ __noinline__ void decide(const StreamParams& p, const CdfParams& cq, 
       const int F = p.F[k];
       const float Ck = p.C[k];
       if (Ck < 1.f && F > 0) {
+        float tvs[kMaxTopK];  // the set's logits, loaded together
+#pragma unroll
+        for (int f = 0; f < kMaxTopK; ++f) tvs[f] = f < F ? __ldcg(&rd->tv[f]) : 0.f;
         double QS = 0.0;
-        for (int f = 0; f < F; ++f) QS += (double)exp2f(fmaf(__ldcg(&rd->tv[f]), cf, -gp.mc_d));
+#pragma unroll
+        for (int f = 0; f < kMaxTopK; ++f)
+          if (f < F) QS += (double)exp2f(fmaf(tvs[f], cf, -gp.mc_d));
         QS /= sq;
         const double gn = 1.0 / (1.0 - (1.0 - (double)Ck) * QS);
         scale_out = gn / sq;
