@@ -773,7 +773,8 @@ __device__ __noinline__ void direct_draw(const CdfParams& p, const float2* bs, i
   constexpr int BE = kVecsPerWarp * VEC;                 // elements per block
   constexpr int E = units_per_stage(ES) * kUnitA;        // elements per stage
   constexpr int PL = BE / 32;                            // elements per lane in a block
-  static_assert(PL % 16 == 0 && PL <= 32, "a lane's run is one or two 16-element halves");
+  static_assert(PL == 8 || PL == 16 || PL == 32, "a lane's run is half, one or two 16-element halves");
+  constexpr int PW = PL < 16 ? 16 : PL;                  // held per lane (zero weights beyond PL)
   const int lane = threadIdx.x & 31;
   if (!SSD_CHK(g < p.groups, p.dbg, 50, g, p.groups)) return;
   const bool tgt = gp.use_t != 0;
@@ -784,6 +785,18 @@ __device__ __noinline__ void direct_draw(const CdfParams& p, const float2* bs, i
   const float dsc = gp.scale_in - gp.scale_out;
   const char* row = tgt ? row_ptr(p.tgt, gp.row_t, p.t_stride, ES) : row_ptr(p.dft, gp.row_d, p.d_stride, ES);
   const int rounds = (nblk + 32 * R - 1) / (32 * R);
+  // the cached set S (lane f < nS: token f, its block and weight difference),
+  // loaded at once
+  int s_blk = -1;
+  float s_d = 0.f;
+  if (lane < nS) {
+    const int tok = __ldcg(&rr->ti[lane]);
+    const float tv = __ldcg(&rr->tv[lane]);
+    if (tok >= 0) {
+      s_blk = (tok / E) * kConsumerWarps + (tok % E) / BE;
+      s_d = dsc * ex2(fmaf(tv, gp.c, -mc));
+    }
+  }
   float v[R];
   auto load_round = [&](int rnd) {
 #pragma unroll
@@ -798,12 +811,11 @@ __device__ __noinline__ void direct_draw(const CdfParams& p, const float2* bs, i
     }
     // the cached set's tokens move from the out-of-S to the in-S weight
     for (int f = 0; f < nS; ++f) {
-      const int tok = __ldcg(&rr->ti[f]);
-      if (tok < 0) continue;
-      const int b = (tok / E) * kConsumerWarps + (tok % E) / BE;
+      const int b = __shfl_sync(0xffffffffu, s_blk, f);
+      const float d = __shfl_sync(0xffffffffu, s_d, f);
+      if (b < 0) continue;
       const int k = b - rnd * 32 * R - lane * R;
       if (k >= 0 && k < R) {
-        const float d = dsc * ex2(fmaf(__ldcg(&rr->tv[f]), gp.c, -mc));
 #pragma unroll
         for (int q = 0; q < R; ++q)
           if (q == k) v[q] = fmaxf(v[q] + d, 0.f);
@@ -881,7 +893,9 @@ __device__ __noinline__ void direct_draw(const CdfParams& p, const float2* bs, i
     const int e_lo = (blk / kConsumerWarps) * E + (blk % kConsumerWarps) * BE;
     const int e_hi = min(p.V, e_lo + BE);
     const int y0 = e_lo + lane * PL;
-    float z[PL], w[PL];
+    float z[PW], w[PW];
+#pragma unroll
+    for (int k = PL; k < PW; ++k) z[k] = w[k] = 0.f;
 #pragma unroll
     for (int k = 0; k < PL; k += VEC) {
       const uintptr_t a = (uintptr_t)(row + (int64_t)(y0 + k) * ES);

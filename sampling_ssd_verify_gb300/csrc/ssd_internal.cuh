@@ -27,6 +27,8 @@ constexpr int kUnitB = 512;                         // elements per unit of the 
 constexpr int kMaxTopK = 16;                        // per-row candidate list (F + 1 <= 16)
 constexpr int kMaxChunkStages = 32;                 // stages of one row chunk (block maxima in smem)
 constexpr int kMaxBlocks = kMaxChunkStages * kConsumerWarps;
+constexpr int kBlkPerLane = kMaxBlocks / 32;            // block maxima per lane of a warp
+static_assert(kMaxBlocks % 32 == 0 && kBlkPerLane <= 32, "block maxima fit one mask per lane");
 constexpr int kMaxGrid = 4096;                      // bound on CTAs of one launch
 constexpr int kTokCache = 4096;                     // draft tokens kept in shared memory
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded waits: 2 s

@@ -362,12 +362,13 @@ struct PieceDesc {
 };
 
 // ---- the top list of a row chunk (epilogue warp) ------------------------------------------
-// Block b of a row chunk is consumer warp b % 16's share of stage s0 + b / 16:
-// vectors [128 w, 128 w + 128) of the stage's aligned interior, plus the
+// Block b of a row chunk is consumer warp b % W's share of stage s0 + b / W
+// (W = kConsumerWarps): vectors [kVecsPerWarp w, kVecsPerWarp (w + 1)) of
+// the stage's aligned interior, plus the
 // unaligned head and tail of the stage for w = 0.  The consumers record each
 // block's maximum and each warp's maximum over the chunk.
 //
-// theta = the R-th largest of the 16 warp maxima: R different warps hold a
+// theta = the R-th largest of the W warp maxima: R different warps hold a
 // logit >= theta, so no logit below it is in the top R.  Every block whose
 // maximum reaches theta is read again (from L2: the chunk was just
 // streamed) and its logits >= theta are offered to the warp list.
@@ -510,11 +511,11 @@ __device__ __forceinline__ void list_block(const StreamParams& p, const char* rp
   }
 }
 
-// The chunk's top list: wm = lane w's warp maximum (lanes >= 16: -inf),
+// The chunk's top list: wm = lane w's warp maximum (lanes >= W: -inf),
 // v[j] = the maximum of block lane + 32 j.
 template <int DT>
 __device__ __noinline__ void chunk_top(const StreamParams& p, int64_t row, int s0, float wm,
-                          const float (&v)[16], WarpList& wl) {
+                          const float (&v)[kBlkPerLane], WarpList& wl) {
   const int lane = threadIdx.x & 31;
   // theta: the R-th largest warp maximum (-inf when fewer than R warps saw data)
   float th = kNegInf;
@@ -538,7 +539,7 @@ __device__ __noinline__ void chunk_top(const StreamParams& p, int64_t row, int s
   // the candidate blocks, lane by lane in order
   unsigned cmask = 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) cmask |= (v[j] != kNegInf && v[j] >= th) ? (1u << j) : 0u;
+  for (int j = 0; j < kBlkPerLane; ++j) cmask |= (v[j] != kNegInf && v[j] >= th) ? (1u << j) : 0u;
   unsigned lanes = __ballot_sync(0xffffffffu, cmask != 0);
   while (lanes) {
     const int L = __ffs(lanes) - 1;
@@ -679,9 +680,10 @@ __device__ __noinline__ void decide(const StreamParams& p, const CdfParams& cq, 
     }
     return;
   }
+  // the draw's parameters, computed by every lane (the same loads, the same
+  // arithmetic); lane 0 stores them
   GroupParams gp;
-  if (lane == 0) {
-    p.accept_len[g] = k;
+  {
     const RowResult* rt = p.rowres + g * p.rpg + k;
     gp.k = k;
     gp.use_t = 1;
@@ -725,6 +727,9 @@ __device__ __noinline__ void decide(const StreamParams& p, const CdfParams& cq, 
     }
     gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)k, 1u, p.round);
     gp.c = cf;
+  }
+  if (lane == 0) {
+    p.accept_len[g] = k;
     p.gparams[g] = gp;
   }
   if (k == K && p.bsum != nullptr) {
@@ -732,8 +737,6 @@ __device__ __noinline__ void decide(const StreamParams& p, const CdfParams& cq, 
     // streaming pass stored for target row K (no ticket: count it as decided
     // first, so that idle producers need not wait for the draw)
     if (lane == 0) mark_decided(p);
-    __syncwarp();
-    gp = load_gp(p.gparams + g);
     direct_draw<DT>(cq, p.bsum + g * p.nblk, p.nblk, gp, g, nullptr, 0);
     return;
   }
@@ -750,12 +753,14 @@ __device__ __noinline__ void saguaro_finish(const StreamParams& p, const CdfPara
                                const RowResult& rr, float cf) {
   const int lane = threadIdx.x & 31;
   const int F = saguaro_F(p, g);
-  if (lane == 0) {
-    if (p.F_rows != nullptr && p.status) {
-      const int f = __ldg(p.F_rows + g);
-      if (f < 0 || f > p.Fmax) atomicOr(p.status, SSD_DEV_BAD_FANOUT);
-    }
-    GroupParams gp;
+  if (lane == 0 && p.F_rows != nullptr && p.status) {
+    const int f = __ldg(p.F_rows + g);
+    if (f < 0 || f > p.Fmax) atomicOr(p.status, SSD_DEV_BAD_FANOUT);
+  }
+  // q''s parameters, computed by every lane (rr is the same in every lane);
+  // lane 0 stores them
+  GroupParams gp;
+  {
     gp.k = 0;
     gp.use_t = 0;
     gp.use_d = 1;
@@ -783,12 +788,11 @@ __device__ __noinline__ void saguaro_finish(const StreamParams& p, const CdfPara
     gp.scale_in = (float)scale_in;
     gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)p.jpos, 2u, p.round);
     gp.c = cf;
-    p.gparams[g] = gp;
   }
+  if (lane == 0) p.gparams[g] = gp;
   if (p.bsum != nullptr) {
-    if (lane == 0) mark_decided(p);
-    __syncwarp();
-    const GroupParams gp = load_gp(p.gparams + g);
+    // counted only where producers wait for queued draws
+    if (lane == 0 && cq.cpg > 0) mark_decided(p);
     direct_draw<DT>(cq, p.bsum + g * p.nblk, p.nblk, gp, g, p.rowres + g, F);
     return;
   }
@@ -1227,9 +1231,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         b.lo = R.lo[lane];
       }
       const int nb = R.nst * kConsumerWarps;
-      float v[16];
+      float v[kBlkPerLane];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kBlkPerLane; ++j) {
         const int bb = lane + 32 * j;
         v[j] = (need > 0 && bb < nb) ? R.bmax[bb] : kNegInf;
       }
@@ -1503,10 +1507,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
 
     if (top) {
-      // The piece's top-list candidates.  theta = the R-th largest of the 16
+      // The piece's top-list candidates.  theta = the R-th largest of the W
       // warp maxima (R warps hold a logit >= theta, so no logit below it is
       // in the top R); each warp reads its own blocks whose maximum reaches
-      // theta again (from L2, just streamed) and lists their logits >= theta.
+      // theta again and lists their logits >= theta.
       if (lane == 0) R.wmax[warp] = wmax;
       consumer_sync();
       float m = lane < kConsumerWarps ? R.wmax[lane] : kNegInf;
