@@ -584,6 +584,11 @@ ssd_status ssd_tree_verify(const ssd_logits* target, const ssd_logits* draft, in
   tp.B = B;
   tp.N = N;
   tp.V = V;
+  // CTAs per tree: the most (up to 8) that keep every tree's cluster resident
+  // at once (one 512-thread CTA per SM)
+  tp.cluster = kTreeMaxCluster;
+  while (tp.cluster > 1 && (int64_t)B * tp.cluster > (int64_t)std::max(num_sms(), 1))
+    tp.cluster >>= 1;
   tp.c = p.c;
   tp.tgt = p.tgt;
   tp.t_stride = p.t_stride;

@@ -215,12 +215,14 @@ struct VerifyParams {
   CdfParams q;
 };
 
-// Tree-draft verification (ssd_tree.cu): one CTA per tree walks it after
-// the streaming pass has normalised every row (row u of tree b: target at
-// rowres[b * 2N + u], draft at rowres[b * 2N + N + u]).
+// Tree-draft verification (ssd_tree.cu): one cluster of `cluster` CTAs per
+// tree walks it after the streaming pass has normalised every row (row u of
+// tree b: target at rowres[b * 2N + u], draft at rowres[b * 2N + N + u]).
 constexpr int kMaxTreeNodes = 256;
+constexpr int kTreeMaxCluster = 8;
 struct TreeParams {
   int B, N, V;
+  int cluster;              // CTAs per tree: 1, 2, 4 or 8
   float c;                  // log2(e) / T
   const void* tgt;
   int64_t t_stride;
