@@ -139,6 +139,50 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---- thread-block clusters ---------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits; the
+// release/acquire pair orders the shared (local and remote) and global
+// accesses made before the barrier with those made after it.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The split form: every CTA arrives at launch and waits before its first
+// store to another CTA's shared memory, so that no store reaches a CTA of the
+// cluster that has not started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// The address of *local in CTA `rank`'s shared memory (shared::cluster window).
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(ra)
+               : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+  return ra;
+}
+// Stores into another CTA's shared memory (addresses from cluster_addr).
+__device__ __forceinline__ void st_cluster_f64(double* local, uint32_t rank, double v) {
+  asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(cluster_addr(local, rank)), "d"(v)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t ra, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
+
 // Relaxed / acquire loads and release stores of 32-bit words that other
 // CTAs of the launch write (draw-queue counters and entries).
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* f) {
@@ -264,6 +308,28 @@ struct Elem<1> {  // fp32
     x[3] = __uint_as_float(v.w);
   }
 };
+
+// A lane's run of VEC elements from y as a 16-byte vector: one load when the
+// row is aligned and the run lies inside it, else element by element (zero
+// bits beyond V).
+template <int DT>
+__device__ __forceinline__ uint4 load_run(const char* row, int y, int V, bool vec) {
+  constexpr int VEC = Elem<DT>::kVec;
+  if (vec && y + VEC <= V) return __ldg(reinterpret_cast<const uint4*>(row) + y / VEC);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if constexpr (DT == 0) {
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k)
+      if (y + k < V) w[k >> 1] |= (uint32_t)__ldg(h + y + k) << (16 * (k & 1));
+  } else {
+    const uint32_t* f = reinterpret_cast<const uint32_t*>(row);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k)
+      if (y + k < V) w[k] = __ldg(f + y + k);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // Element k (runtime index) of a 16-byte vector, without spilling the vector.
 template <int DT>

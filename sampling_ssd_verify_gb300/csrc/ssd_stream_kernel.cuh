@@ -650,6 +650,80 @@ __device__ __forceinline__ void mark_decided(const StreamParams& p) {
   atomicAdd(p.decided, 1);
 }
 
+// The bonus draw's parameters for sequence g decided with accept length k:
+// the residual (p_k - q'_k)^+ (q' biased by the Saguaro set of draft row k),
+// or p_K when every draft was accepted.  Every lane of a warp computes the
+// same value from the same loads.
+__device__ __forceinline__ GroupParams draw_params(const StreamParams& p, int64_t g, int k,
+                                                   float cf) {
+  const int K = p.K;
+  GroupParams gp;
+  const RowResult* rt = p.rowres + g * p.rpg + k;
+  gp.k = k;
+  gp.use_t = 1;
+  gp.row_t = g * (int64_t)(K + 1) + k;
+  gp.mc_t = __ldcg(&rt->mc);
+  gp.inv_st = (float)(1.0 / __ldcg(&rt->s));
+  gp.sign_d = -1;
+  gp.theta = kPosInf;
+  gp.itheta = -1;
+  if (k < K) {
+    const RowResult* rd = p.rowres + g * p.rpg + p.nt + k;
+    gp.use_d = 1;
+    gp.row_d = g * (int64_t)p.Kq + k;
+    gp.mc_d = __ldcg(&rd->mc);
+    const double sq = __ldcg(&rd->s);
+    double scale_out = 1.0 / sq, scale_in = 1.0 / sq;
+    const int F = p.F[k];
+    const float Ck = p.C[k];
+    if (Ck < 1.f && F > 0) {
+      float tvs[kMaxTopK];  // the set's logits, loaded together
+#pragma unroll
+      for (int f = 0; f < kMaxTopK; ++f) tvs[f] = f < F ? __ldcg(&rd->tv[f]) : 0.f;
+      double QS = 0.0;
+#pragma unroll
+      for (int f = 0; f < kMaxTopK; ++f)
+        if (f < F) QS += (double)exp2f(fmaf(tvs[f], cf, -gp.mc_d));
+      QS /= sq;
+      const double gn = 1.0 / (1.0 - (1.0 - (double)Ck) * QS);
+      scale_out = gn / sq;
+      scale_in = gn * (double)Ck / sq;
+      gp.theta = __ldcg(&rd->tv[F - 1]);
+      gp.itheta = __ldcg(&rd->ti[F - 1]);
+    }
+    gp.scale_out = (float)scale_out;
+    gp.scale_in = (float)scale_in;
+  } else {
+    gp.use_d = 0;
+    gp.row_d = 0;
+    gp.mc_d = 0.f;
+    gp.scale_out = gp.scale_in = 0.f;
+  }
+  gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)k, 1u, p.round);
+  gp.c = cf;
+  return gp;
+}
+
+// The outputs of greedy sequence g with accept length k (one lane): the
+// bonus is target row k's argmax; no draw (its parameters say so).
+__device__ __forceinline__ void greedy_outcome(const StreamParams& p, int64_t g, int k) {
+  p.accept_len[g] = k;
+  const int t = __ldcg(&p.rowres[g * p.rpg + k].ti[0]);
+  p.bonus[g] = t;
+  if (p.resid_mass) p.resid_mass[g] = 1.f;
+  if (p.rc.table != nullptr)  // the round's cache: look the outcome (k, t) up
+    round_outcome(static_cast<const Slot*>(p.rc.table), p.rc.cap, g, k, t, p.B, p.rc.branch,
+                  p.rc.all_hit, p.rc.cnt);
+  if (p.T_rows != nullptr && p.status) {
+    const float T = __ldg(p.T_rows + g);
+    if (T != 0.f) atomicOr(p.status, SSD_DEV_BAD_TEMPERATURE);
+  }
+  GroupParams gp = {};
+  gp.theta = kPosInf;
+  gp.itheta = -1;
+  p.gparams[g] = gp;
+}
+
 // Sequence g is decided with accept length k (warp of the deciding CTA):
 // write k, then either the greedy outputs, a direct draw of p_K from the
 // streaming pass's block sums, or the draw's chunks to the ticket queue.
@@ -661,73 +735,14 @@ __device__ __noinline__ void decide(const StreamParams& p, const CdfParams& cq, 
   if (!SSD_CHK(g < p.B && k >= 0 && k <= K, p.dbg, 8, g, k)) return;
   if (seq_greedy(p, g)) {
     if (lane == 0) {
-      p.accept_len[g] = k;
-      const int t = __ldcg(&p.rowres[g * p.rpg + k].ti[0]);
-      p.bonus[g] = t;
-      if (p.resid_mass) p.resid_mass[g] = 1.f;
-      if (p.rc.table != nullptr)  // the round's cache: look the outcome (k, t) up
-        round_outcome(static_cast<const Slot*>(p.rc.table), p.rc.cap, g, k, t, p.B, p.rc.branch,
-                      p.rc.all_hit, p.rc.cnt);
-      if (p.T_rows != nullptr && p.status) {
-        const float T = __ldg(p.T_rows + g);
-        if (T != 0.f) atomicOr(p.status, SSD_DEV_BAD_TEMPERATURE);
-      }
-      GroupParams gp = {};
-      gp.theta = kPosInf;
-      gp.itheta = -1;
-      p.gparams[g] = gp;
+      greedy_outcome(p, g, k);
       mark_decided(p);
     }
     return;
   }
   // the draw's parameters, computed by every lane (the same loads, the same
   // arithmetic); lane 0 stores them
-  GroupParams gp;
-  {
-    const RowResult* rt = p.rowres + g * p.rpg + k;
-    gp.k = k;
-    gp.use_t = 1;
-    gp.row_t = g * (int64_t)(K + 1) + k;
-    gp.mc_t = __ldcg(&rt->mc);
-    gp.inv_st = (float)(1.0 / __ldcg(&rt->s));
-    gp.sign_d = -1;
-    gp.theta = kPosInf;
-    gp.itheta = -1;
-    if (k < K) {
-      const RowResult* rd = p.rowres + g * p.rpg + p.nt + k;
-      gp.use_d = 1;
-      gp.row_d = g * (int64_t)p.Kq + k;
-      gp.mc_d = __ldcg(&rd->mc);
-      const double sq = __ldcg(&rd->s);
-      double scale_out = 1.0 / sq, scale_in = 1.0 / sq;
-      const int F = p.F[k];
-      const float Ck = p.C[k];
-      if (Ck < 1.f && F > 0) {
-        float tvs[kMaxTopK];  // the set's logits, loaded together
-#pragma unroll
-        for (int f = 0; f < kMaxTopK; ++f) tvs[f] = f < F ? __ldcg(&rd->tv[f]) : 0.f;
-        double QS = 0.0;
-#pragma unroll
-        for (int f = 0; f < kMaxTopK; ++f)
-          if (f < F) QS += (double)exp2f(fmaf(tvs[f], cf, -gp.mc_d));
-        QS /= sq;
-        const double gn = 1.0 / (1.0 - (1.0 - (double)Ck) * QS);
-        scale_out = gn / sq;
-        scale_in = gn * (double)Ck / sq;
-        gp.theta = __ldcg(&rd->tv[F - 1]);
-        gp.itheta = __ldcg(&rd->ti[F - 1]);
-      }
-      gp.scale_out = (float)scale_out;
-      gp.scale_in = (float)scale_in;
-    } else {
-      gp.use_d = 0;
-      gp.row_d = 0;
-      gp.mc_d = 0.f;
-      gp.scale_out = gp.scale_in = 0.f;
-    }
-    gp.u = uniform24(p.seeds[g], (uint32_t)g, (uint32_t)k, 1u, p.round);
-    gp.c = cf;
-  }
+  const GroupParams gp = draw_params(p, g, k, cf);
   if (lane == 0) {
     p.accept_len[g] = k;
     p.gparams[g] = gp;
@@ -802,6 +817,50 @@ __device__ __noinline__ void saguaro_finish(const StreamParams& p, const CdfPara
   }
 }
 
+// The bonus guesses of draft row j of group g (one warp; lane l < R of wl
+// holds list entry l): top-(F_j+1) minus the sampled token, truncated to F_j;
+// lane f writes guess f (entry f of the list, or f + 1 once the drafted
+// token is passed), and, with the round's cache (table_ready: cleared),
+// inserts its key (sequence, position, guess) -> index in the guesses array.
+__device__ __forceinline__ void row_guesses(const StreamParams& p, int64_t g, int j,
+                                            const RowResult& rr, const WarpList& wl, int need,
+                                            float c, float MC, bool table_ready) {
+  const int lane = threadIdx.x & 31;
+  if (p.guesses != nullptr) {
+    const bool greedy = p.mode == kModeVerify && seq_greedy(p, g);
+    const int F = p.F[j];
+    const unsigned hitx =
+        __ballot_sync(0xffffffffu, lane < F + 1 && lane < need && wl.li == rr.x && rr.x >= 0);
+    const int sx = hitx ? __ffs(hitx) - 1 : 32;
+    const int e = lane < sx ? lane : lane + 1;
+    const float ev = __shfl_sync(0xffffffffu, wl.lv, e & 31);
+    const int ei = __shfl_sync(0xffffffffu, wl.li, e & 31);
+    const int i0 = __shfl_sync(0xffffffffu, wl.li, 0);
+    const bool valid = lane < F && e < need && ev != kNegInf;
+    const int64_t o = (g * p.nd + j) * (int64_t)p.Fmax;
+    if (lane < p.Fmax && SSD_CHK(o + lane < (int64_t)p.B * p.nd * p.Fmax, p.dbg, 7, o + lane, lane)) {
+      p.guesses[o + lane] = valid ? ei : -1;
+      if (p.guess_q)
+        p.guess_q[o + lane] = !valid ? 0.f
+                              : greedy ? (ei == i0 ? 1.f : 0.f)
+                                       : ex2(fmaf(ev, c, -MC)) / (float)rr.s;
+    }
+  }
+  if (p.rc.table != nullptr && p.guesses != nullptr && p.F[j] > 0 && table_ready) {
+    const int F = p.F[j];
+    int sx = kMaxTopK;
+    for (int k = F; k >= 0; --k)
+      if (rr.ti[k] == rr.x) sx = k;
+    if (lane < F) {
+      const int e = lane < sx ? lane : lane + 1;
+      const int tok = e < kMaxTopK ? rr.ti[e] : -1;
+      if (tok >= 0)
+        cache_insert(static_cast<Slot*>(p.rc.table), p.rc.cap, pack_key((int)g, j, tok),
+                     (int)((g * p.nd + j) * p.Fmax + lane), p.status);
+    }
+  }
+}
+
 // Finalise row `row` from the merged (M, MC, S) and top list (lane l < R
 // holds entry l).  Writes the row's result, its guesses and cache keys, then
 // counts the row into its position (verify) or draws (Saguaro).
@@ -848,51 +907,16 @@ __device__ __noinline__ void finalize_row(const StreamParams& p, const CdfParams
                     p.dbg, 4, row, x) ? Elem<DT>::load_cg(rp, x) : 0.f;
   }
   if (lane == 0 && SSD_CHK(row < p.NR, p.dbg, 5, row, p.NR)) p.rowres[row] = rr;
-  // bonus guesses: top-(F_j+1) minus the sampled token, truncated to F_j;
-  // lane f writes guess f (entry f of the list, or f + 1 once the drafted
-  // token is passed)
-  if (!is_t && p.guesses != nullptr) {
-    const bool greedy = p.mode == kModeVerify && seq_greedy(p, g);
-    const int F = p.F[j];
-    const unsigned hitx =
-        __ballot_sync(0xffffffffu, lane < F + 1 && lane < need && wl.li == rr.x && rr.x >= 0);
-    const int sx = hitx ? __ffs(hitx) - 1 : 32;
-    const int e = lane < sx ? lane : lane + 1;
-    const float ev = __shfl_sync(0xffffffffu, wl.lv, e & 31);
-    const int ei = __shfl_sync(0xffffffffu, wl.li, e & 31);
-    const int i0 = __shfl_sync(0xffffffffu, wl.li, 0);
-    const bool valid = lane < F && e < need && ev != kNegInf;
-    const int64_t o = (g * p.nd + j) * (int64_t)p.Fmax;
-    if (lane < p.Fmax && SSD_CHK(o + lane < (int64_t)p.B * p.nd * p.Fmax, p.dbg, 7, o + lane, lane)) {
-      p.guesses[o + lane] = valid ? ei : -1;
-      if (p.guess_q)
-        p.guess_q[o + lane] = !valid ? 0.f
-                              : greedy ? (ei == i0 ? 1.f : 0.f)
-                                       : ex2(fmaf(ev, c, -MC)) / (float)rr.s;
-    }
-  }
-  if (!is_t && p.rc.table != nullptr && p.guesses != nullptr && p.F[j] > 0) {
-    // the round's cache: guess f of this row (entry f of the list, or f + 1
-    // once the drafted token is passed) -> key (sequence, position, guess),
-    // value its index in the guesses array; one lane per guess, after every
-    // CTA has cleared its slice of the table
-    const int F = p.F[j];
-    if (!*cleared) {
+  if (!is_t) {
+    bool ready = p.rc.table == nullptr || p.guesses == nullptr || p.F[j] == 0 || *cleared;
+    if (!ready) {
+      // the round's cache takes keys after every CTA has cleared its slice
       int ok = 0;
       if (lane == 0)
         ok = count_wait(p.rc.cleared, (int)gridDim.x * kEpilogueWarps, s_err, p.status);
-      *cleared = __shfl_sync(0xffffffffu, ok, 0) != 0;
+      *cleared = ready = __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
-    int sx = kMaxTopK;
-    for (int k = F; k >= 0; --k)
-      if (rr.ti[k] == rr.x) sx = k;
-    if (*cleared && lane < F) {
-      const int e = lane < sx ? lane : lane + 1;
-      const int tok = e < kMaxTopK ? rr.ti[e] : -1;
-      if (tok >= 0)
-        cache_insert(static_cast<Slot*>(p.rc.table), p.rc.cap, pack_key((int)g, j, tok),
-                     (int)((g * p.nd + j) * p.Fmax + lane), p.status);
-    }
+    row_guesses(p, g, j, rr, wl, need, c, MC, ready);
   }
   // orders every lane's stores (results, guesses, cache keys and values)
   // before lane 0's release arrival below
@@ -1421,7 +1445,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     const int nst = (int)((pu1 - pu0 + ups - 1) / ups);  // stages of the piece
     for (int s = 0; s < nst; ++s) {
       if (s != 0) mbar_wait(full + slot, phase, &s_err, p.status);
-      const int nvec = s_sd[slot].nvec;
+      // the stage's description and data are read first and the slot is
+      // released before the arithmetic, so that the producer refills it
+      // while this stage is reduced
+      const StageDesc st = s_sd[slot];
+      const int nvec = st.nvec;
       const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
       const int vb = warp * kVecsPerWarp + lane;
       uint4 raw[kVpt];
@@ -1436,6 +1464,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         for (int k = 0; k < kVpt; ++k)
           raw[k] = (vb + 32 * k < nvec && SSD_CHK(vb + 32 * k < kStageVecs, p.dbg, 10, vb, nvec))
                        ? sv[vb + 32 * k] : pad;
+      }
+      if (xtok >= 0 && lane == 0) {
+        // the row's draft-token logit, from this warp's block of the stage
+        const int xe = xtok - st.ei0;
+        if (xe >= warp * kVecsPerWarp * VEC && xe < min((warp + 1) * kVecsPerWarp, nvec) * VEC)
+          R.zx = Elem<DT>::smem(ring + slot * kStageBytes, xe);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + slot);
+      if (++slot == kStagesA) {
+        slot = 0;
+        phase ^= 1u;
       }
       float x[N];
 #pragma unroll
@@ -1464,7 +1504,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       }
       // unaligned head / tail elements (fewer than 32) by warp 0, from global memory
       if (warp == 0) {
-        const StageDesc st = s_sd[slot];
         const int ei0 = st.ei0;
         const int hc = nvec > 0 ? ei0 - st.e0 : st.e1 - st.e0;
         const int ei1 = ei0 + nvec * VEC;
@@ -1491,18 +1530,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         wmax = fmaxf(wmax, bm);
         if (lane == s) mybm = bm;
         if (lane == 0) R.bmax[s * kConsumerWarps + warp] = bm;
-      }
-      if (xtok >= 0 && lane == 0) {
-        // the row's draft-token logit, from this warp's block of the stage
-        const int xe = xtok - s_sd[slot].ei0;
-        if (xe >= warp * kVecsPerWarp * VEC && xe < min((warp + 1) * kVecsPerWarp, nvec) * VEC)
-          R.zx = Elem<DT>::smem(ring + slot * kStageBytes, xe);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty + slot);
-      if (++slot == kStagesA) {
-        slot = 0;
-        phase ^= 1u;
       }
     }
 

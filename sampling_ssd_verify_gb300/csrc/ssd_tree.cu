@@ -55,39 +55,6 @@ struct TreeRing {
   static_assert(kStages >= 2, "the ring holds at least two stages");
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster arrives, then waits; the
-// release/acquire pair orders the shared (local and remote) and global
-// accesses made before the barrier with those made after it.
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// The split form: every CTA arrives at launch and waits before its first
-// store to another CTA's shared memory, so that no store reaches a CTA of the
-// cluster that has not started.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-
-// Store v at the address of *local in CTA `rank`'s shared memory.
-__device__ __forceinline__ void st_cluster_f64(double* local, uint32_t rank, double v) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(ra), "d"(v) : "memory");
-}
-
 // The weight of one element: p_u(y) (no draft term) or (p_u(y) - s q_u(y))^+,
 // with p = exp2(fl(z c - mc_t)) inv_st and s q = exp2(fl(z c - mc_d)) scale --
 // the same expressions as the bonus draw's weight (ssd_cdf_dev.cuh).
@@ -100,28 +67,6 @@ __device__ __forceinline__ float pass_weight(const PassW& w, float zt, float zd)
   const float pt = ex2(fmaf(zt, w.c, -w.mc_t)) * w.inv_st;
   if (!USE_D) return pt;
   return fmaxf(pt - ex2(fmaf(zd, w.c, -w.mc_d)) * w.scale, 0.f);
-}
-
-// A lane's run of VEC elements from y as a 16-byte vector: one load when the
-// row is aligned and the run lies inside it, else element by element (zero
-// bits beyond V).
-template <int DT>
-__device__ __forceinline__ uint4 load_run(const char* row, int y, int V, bool vec) {
-  constexpr int VEC = Elem<DT>::kVec;
-  if (vec && y + VEC <= V) return __ldg(reinterpret_cast<const uint4*>(row) + y / VEC);
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  if constexpr (DT == 0) {
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
-#pragma unroll
-    for (int k = 0; k < VEC; ++k)
-      if (y + k < V) w[k >> 1] |= (uint32_t)__ldg(h + y + k) << (16 * (k & 1));
-  } else {
-    const uint32_t* f = reinterpret_cast<const uint32_t*>(row);
-#pragma unroll
-    for (int k = 0; k < VEC; ++k)
-      if (y + k < V) w[k] = __ldg(f + y + k);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // The weight sum of unit `un` (elements un * 512 ...), in every lane.  Lane
