@@ -75,6 +75,31 @@ def test_tree_verify_matches_oracle(orc, tree, wl, B, V, dtype):
     assert int(status.item()) == 0
 
 
+@pytest.mark.parametrize("B,V,dtype", [(70, 4099, "bf16"), (36, 1000, "f32")],
+                         ids=["two-CTA-clusters-unaligned-rows", "four-CTA-clusters"])
+def test_tree_cluster_sizes(orc, B, V, dtype):
+    """Batches that give the walk clusters of 2 and 4 CTAs per tree; V = 4099
+    bf16 rows alternate between 16-byte aligned (bulk-copy ring) and not
+    (plain loads); V = 1000 (two units) leaves a partial last unit and two of
+    the four CTAs of a cluster without a share of the rows."""
+    torch, dev = torch_dev()
+    w = WORKLOADS["c3"]
+    parent = np.array(TREES["uneven-11"], dtype=np.int32)
+    N = len(parent)
+    tgt, dft, seeds = _tree_batch(w, B, N, V, dtype, seed=V)
+    tg, dg = upload(tgt, dtype), upload(dft, dtype)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for rnd in (2, 3):
+        tok = orc.tree_draft(dft, parent, seeds, rnd, w.T, nthreads=16)
+        g = ssd.tree_verify(tg, dg, parent, i32(tok), seeds_t(seeds), rnd, w.T,
+                            dev_status=status)
+        g = {k: v.cpu().numpy() for k, v in g.items()}
+        o = orc.tree_verify(tgt, dft, parent, tok, seeds, rnd, w.T, nthreads=16)
+        compare_tree(g, o)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
 def test_chain_tree_equals_linear_verify(orc):
     """A chain verified as a tree gives ssd_verify's accept lengths and bonus
     tokens at C = 1, bit for bit."""
