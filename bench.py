@@ -576,6 +576,77 @@ def run_fanout_ablation(args):
                       "data": "synthetic", "rows": rows}))
 
 
+TREES = {"chain-4": [-1, 0, 1, 2, 3], "binary-depth-3": [-1, 0, 0, 1, 1, 2, 2],
+         "wide-3x2": [-1, 0, 0, 0, 1, 1, 2, 2, 3, 3]}
+
+
+def run_tree(args):
+    """ssd_tree_verify on trees of the workload's rows (row u of a tree is
+    the generator's position u; child v's token drawn from its parent's draft
+    row by the library's sampler with C = 1, counter (b, v - 1, 2, round 0)),
+    timed with CUDA events over back-to-back calls.  Prints one JSON line:
+    trees/s and the roofline of the call's algorithmic bytes (every node's
+    target and draft row read once)."""
+    import torch
+
+    import sampling_ssd_verify_gb300 as ssd
+    from ssd_inputs import WORKLOADS, make_batch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ssd.build()
+    w = WORKLOADS[args.workload]
+    parent = TREES[args.tree]
+    N = len(parent)
+    B = args.batch or w.B
+    V = args.vocab or w.V
+    bt = make_batch(w, B=B, V=V, K=N - 1, seed=w.seed)
+    if w.dtype == "bf16":
+        tg = torch.from_numpy(bt["target"].view(np.int16)).to(dev).view(torch.bfloat16)
+        dg = torch.from_numpy(np.ascontiguousarray(bt["draft"][:, :N]).view(np.int16)).to(dev)
+        dg = dg.view(torch.bfloat16)
+    else:
+        tg = torch.from_numpy(bt["target"]).to(dev)
+        dg = torch.from_numpy(np.ascontiguousarray(bt["draft"][:, :N])).to(dev)
+    seeds = torch.from_numpy(bt["seeds"].view(np.int64)).to(dev)
+    tok = torch.full((B, N), -1, dtype=torch.int32, device=dev)
+    for v in range(1, N):
+        tok[:, v] = ssd.saguaro_sample(dg[:, parent[v], :], w.T, 1.0, 0, seeds, v - 1, 0,
+                                       guesses=False, qprime=False)["token"]
+    ws = torch.empty(ssd.lib().ssd_tree_workspace_size(B, N, V), dtype=torch.uint8, device=dev)
+    out = {}
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    f = lambda i: ssd.tree_verify(tg, dg, parent, tok, seeds, i, w.T, workspace=ws, out=out,
+                                  dev_status=status)
+    for i in range(args.warmup):
+        f(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        f(1000 + i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    es = 2 if w.dtype == "bf16" else 4
+    alg = B * N * 2 * V * es
+    hbm_peak, peak_kind = peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    print(json.dumps({"metric": "tree drafts verified per second", "value": B / (ms * 1e-3),
+                      "unit": "trees/s", "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": ms, "dtype": w.dtype, "data": "synthetic",
+                      "config": {"workload": w.name, "tree": args.tree, "parent": parent,
+                                 "B": B, "N": N, "V": V, "T": w.T,
+                                 "accept_mean": float(out["accept_len"].float().mean().item()),
+                                 "l2": "inputs larger than L2 (no flush)" if alg > 129e6 else
+                                       "inputs smaller than L2"},
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                                   "unit": "GB/s", "frac": achieved / hbm_peak,
+                                   "algorithmic_bytes_per_call": alg, "peak_kind": peak_kind,
+                                   "launches_per_call": 2},
+                      "status": int(status.item())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -594,9 +665,16 @@ def main():
     ap.add_argument("--rounds", type=int, default=64, help="rounds per ablation cell")
     ap.add_argument("--ablation", choices=["fanout"], default=None,
                     help="instead of the benchmark: geometric vs uniform fan-out hit rates")
+    ap.add_argument("--tree", choices=sorted(TREES), default=None,
+                    help="instead of the benchmark: tree-draft verification of that shape")
     args = ap.parse_args()
     if args.ablation == "fanout":
         run_fanout_ablation(args)
+        return
+    if args.tree:
+        args.steps = 100 if args.steps is None else args.steps
+        args.warmup = 5 if args.warmup is None else max(3, args.warmup)
+        run_tree(args)
         return
     if args.impl == "reference":
         args.steps = 3 if args.steps is None else args.steps
