@@ -100,6 +100,32 @@ def test_tree_cluster_sizes(orc, B, V, dtype):
     assert int(status.item()) == 0
 
 
+@pytest.mark.parametrize("shape", ["root-only", "one-edge", "star-255", "chain-255"])
+def test_tree_extreme_shapes(orc, shape):
+    """The degenerate and the largest trees: a root alone (the bonus from p_0,
+    no test), one edge, a root with 255 children (up to 254 residual passes
+    at one node) and a chain of 256 nodes (depth 255)."""
+    torch, dev = torch_dev()
+    N = {"root-only": 1, "one-edge": 2, "star-255": 256, "chain-255": 256}[shape]
+    if shape == "star-255":
+        parent = np.array([-1] + [0] * (N - 1), dtype=np.int32)
+    else:
+        parent = np.arange(-1, N - 1, dtype=np.int32)
+    w = WORKLOADS["c1"]
+    B, V = 3, 1000
+    w = dataclasses.replace(w, V=V)
+    tgt, dft, seeds = _tree_batch(w, B, N, V, "f32", seed=N)
+    tg, dg = upload(tgt, "f32"), upload(dft, "f32")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok = orc.tree_draft(dft, parent, seeds, 1, w.T, nthreads=4)
+    g = ssd.tree_verify(tg, dg, parent, i32(tok), seeds_t(seeds), 1, w.T, dev_status=status)
+    g = {k: v.cpu().numpy() for k, v in g.items()}
+    o = orc.tree_verify(tgt, dft, parent, tok, seeds, 1, w.T, nthreads=4)
+    compare_tree(g, o)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
 def test_chain_tree_equals_linear_verify(orc):
     """A chain verified as a tree gives ssd_verify's accept lengths and bonus
     tokens at C = 1, bit for bit."""
