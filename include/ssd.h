@@ -116,8 +116,14 @@ int ssd_version(void);
  * 1, and guess_q is 1 for the draft argmax and 0 for other guesses; no
  * uniform is drawn.
  *
- * target      [B, K+1, V] logits: row (b, i) is row b*(K+1)+i.
+ * target      [B, K+1, V] logits: row (b, i) is row b*(K+1)+i.  Target rows
+ *             past a known rejection of their sequence are not read: no
+ *             output depends on p_i for i > k (the accept tests stop at the
+ *             first rejection, [SD-7.3] §7.3.3); a row whose sequence is not
+ *             yet decided when its turn comes is read (see
+ *             ssd_verify_skipped_bytes).
  * draft       [B, Kq, V] logits, Kq in {K, K+1}: row (b, j) is row b*Kq+j.
+ *             Every draft row is read (the guesses of every position).
  *             Verification reads draft rows 0..K-1; row K (when Kq = K+1)
  *             only feeds the guesses for the all-accepted outcome.
  * draft_tokens device [B, K] int32.
@@ -144,6 +150,22 @@ ssd_status ssd_verify(const ssd_logits* target, const ssd_logits* draft, int B, 
                       int32_t* bonus, float* resid_mass, int32_t* guesses, float* guess_q,
                       int Fmax, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                       void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ssd_verify_skipped_bytes -- the bytes of target rows that the last call of
+ * ssd_verify, ssd_verify_ck, ssd_verify_ex or ssd_verify_round on `workspace`
+ * did not read (rows past a rejection already known when their turn came).
+ * A measurement aid: the logits streamed by that call are the target and
+ * draft bytes minus this count.
+ *
+ * workspace   the call's workspace (256-byte aligned) and its size; B, K,
+ *             Kq, V and dtype (ssd_dtype) those of the call.
+ * out         device uint64 out, written in stream order after the call.
+ * Errors: SSD_ERR_INVALID_ARG (bad sizes, null pointers), SSD_ERR_WORKSPACE
+ * (smaller than ssd_verify_workspace_size).  Enqueues one 8-byte copy.
+ * ------------------------------------------------------------------------- */
+ssd_status ssd_verify_skipped_bytes(const void* workspace, size_t workspace_bytes, int B, int K,
+                                    int Kq, int V, int dtype, uint64_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------
  * ssd_verify_ck -- ssd_verify with one Saguaro factor per draft position.

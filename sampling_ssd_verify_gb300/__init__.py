@@ -63,6 +63,7 @@ _SIGS = {
     "ssd_status_string": ([_i], ctypes.c_char_p),
     "ssd_version": ([], _i),
     "ssd_verify_workspace_size": ([_i, _i, _i, _i], _sz),
+    "ssd_verify_skipped_bytes": ([_vp, _sz, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "ssd_verify": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32, _vp,
                     ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "ssd_verify_ck": ([_LP, _LP, _i, _i, _i, _i, ctypes.c_float, _vp, _vp, ctypes.c_uint32, _vp,
@@ -304,6 +305,20 @@ def verify_round(target, draft, draft_tokens, seeds, round_, fanout, C=1.0, T=1.
                             _dev_ptr(dev_status), _stream(stream))
     _check(st, "ssd_verify_round")
     return o
+
+
+def verify_skipped_bytes(workspace, target, K, Kq, stream=None):
+    """ssd_verify_skipped_bytes: the bytes of target rows the last verify
+    call on `workspace` (target [B, K+1, V]) did not read, as a Python int
+    (synchronises the stream)."""
+    torch = _torch()
+    B, V = target.shape[0], target.shape[-1]
+    dt = SSD_BF16 if target.dtype == torch.bfloat16 else SSD_F32
+    out = torch.zeros(1, dtype=torch.int64, device=workspace.device)
+    st = lib().ssd_verify_skipped_bytes(_dev_ptr(workspace), workspace.numel(), B, K, Kq, V, dt,
+                                        _dev_ptr(out), _stream(stream))
+    _check(st, "ssd_verify_skipped_bytes")
+    return int(out.item())
 
 
 def verify_host(target, draft, draft_tokens, seeds, round_, fanout=None, C=1.0, T=1.0,

@@ -172,6 +172,7 @@ ssd_status setup(const ssd_logits* target, const ssd_logits* draft, int groups, 
   p.dq_tail = reinterpret_cast<unsigned int*>(w8 + 3 * kCtrStride);
   p.dq_head = reinterpret_cast<unsigned int*>(w8 + 4 * kCtrStride);
   p.decided = reinterpret_cast<int*>(w8 + 5 * kCtrStride);
+  p.skipped = w8 + 6 * kCtrStride;
   p.partials = reinterpret_cast<RowPartial*>(ws + L.part_off);
   p.rowres = reinterpret_cast<RowResult*>(ws + L.rowres_off);
   p.gparams = reinterpret_cast<GroupParams*>(ws + L.gp_off);
@@ -284,6 +285,23 @@ size_t ssd_verify_workspace_size(int B, int K, int Kq, int V) {
   if (B < 1 || K < 1 || K > SSD_MAX_K || (Kq != K && Kq != K + 1) || V < 2 || V > SSD_MAX_V)
     return 0;
   return layout_bytes(B, K + 1 + Kq, K, V, true, true);
+}
+
+ssd_status ssd_verify_skipped_bytes(const void* workspace, size_t workspace_bytes, int B, int K,
+                                    int Kq, int V, int dtype, uint64_t* out, void* stream) {
+  if (B < 1 || K < 1 || K > SSD_MAX_K || (Kq != K && Kq != K + 1) || V < 2 || V > SSD_MAX_V ||
+      (dtype != SSD_BF16 && dtype != SSD_F32) || out == nullptr)
+    return SSD_ERR_INVALID_ARG;
+  if (workspace == nullptr || ((uintptr_t)workspace & 255) != 0 ||
+      workspace_bytes < ssd_verify_workspace_size(B, K, Kq, V))
+    return SSD_ERR_WORKSPACE;
+  // the counter's place in the layout the call used (the counters do not
+  // depend on the block-sum room)
+  const WsLayout L = layout_for(B, K + 1 + Kq, K, V, esize_of(dtype), true, false);
+  const char* ctr = static_cast<const char*>(workspace) + L.cnt_off + L.ctr_off +
+                    6 * kCtrStride * sizeof(unsigned long long);
+  return cuda_status(cudaMemcpyAsync(out, ctr, sizeof(uint64_t), cudaMemcpyDeviceToDevice,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 size_t ssd_topf_workspace_size(int B, int Kq, int V) {

@@ -185,6 +185,11 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t ra, uint32_t v) {
 
 // Relaxed / acquire loads and release stores of 32-bit words that other
 // CTAs of the launch write (draw-queue counters and entries).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* f) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+  return v;
+}
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* f) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");

@@ -165,6 +165,7 @@ struct StreamParams {
   unsigned int* dq_tail;
   unsigned int* dq_head;
   int* decided;             // groups whose draw is queued or done
+  unsigned long long* skipped;  // bytes of target rows not streamed (past a rejection)
   int32_t* status;
   // bounds of the inputs and the debug record (used by SSD_CHECKS builds)
   const char* t_lo;
@@ -277,7 +278,7 @@ inline WsLayout ws_layout(int groups, int rpg, int K, int V, int esize, int nch,
   // arrivals [groups * (K+1)], all-accepted events [groups], draw tickets
   // [groups * cpg]; then 8-byte words: sequence states [groups], the chunk
   // counter, round-cache outcomes, round-cache clearing, queue tail / head,
-  // decided groups
+  // decided groups, bytes of target rows skipped
   L.o_row_cnt = 0;
   L.o_grp_cnt = L.o_row_cnt + (size_t)L.NR;
   L.o_pair = L.o_grp_cnt + (size_t)groups;
@@ -289,7 +290,7 @@ inline WsLayout ws_layout(int groups, int rpg, int K, int V, int esize, int nch,
   // each 8-byte counter on its own 128-byte line: CTAs poll some of them
   // while others are incremented
   L.ctr_off = ((L.o_state + (size_t)groups) * 8 + 127) & ~(size_t)127;
-  L.cnt_bytes = align256(L.ctr_off + 6 * kCtrStride * sizeof(unsigned long long));
+  L.cnt_bytes = align256(L.ctr_off + 7 * kCtrStride * sizeof(unsigned long long));
   L.part_off = L.cnt_bytes;
   const size_t slots = nch > 1 ? (size_t)L.NR * nch : 1;
   L.rowres_off = L.part_off + align256(slots * sizeof(RowPartial));

@@ -569,6 +569,49 @@ __device__ __forceinline__ void fold_partial(SAcc& a, const RowPartial* pp, floa
   }
 }
 
+// ---- target rows past a rejection ---------------------------------------------------------
+// No output depends on target row j of a sequence once one of its positions
+// before j is rejected: the first rejection, which decides the sequence, is
+// then before j, and the accept tests stop there ([SD-7.3] §7.3.3).  Draft
+// rows always stream (their top lists give the guesses of every position).
+// The producer reads the sequence's state word when it fetches a chunk id
+// and drops the chunk when it is such a row; a state read too early only
+// streams a row that is not needed.
+
+// The state word of row chunk c's sequence when c is a target row past
+// position 0 of a verify launch (loaded now, used at the next claim), else 0.
+__device__ __forceinline__ unsigned long long chunk_state(const StreamParams& p, long long c,
+                                                          long long nS) {
+  if (p.mode != kModeVerify || c >= nS) return 0ull;
+  int64_t row, pu0, pu1;
+  int kch;
+  chunk_geom(p, c, row, kch, pu0, pu1);
+  const int64_t g = row / p.rpg;
+  const int jr = (int)(row - g * p.rpg);
+  if (jr == 0 || jr >= p.nt) return 0ull;
+  return ld_relaxed_u64(p.seq_state + g);
+}
+
+// Whether row chunk c is a target row past a rejection recorded in st; if
+// so its bytes are added to the launch's count of bytes not streamed.
+template <int DT>
+__device__ __forceinline__ bool chunk_past_rejection(const StreamParams& p, long long c,
+                                                     unsigned long long st) {
+  if (st >> 32 == 0ull) return false;
+  int64_t row, pu0, pu1;
+  int kch;
+  chunk_geom(p, c, row, kch, pu0, pu1);
+  const int64_t g = row / p.rpg;
+  const int jr = (int)(row - g * p.rpg);
+  if (jr == 0 || jr >= p.nt) return false;
+  const unsigned below = jr >= 32 ? 0xffffffffu : ((1u << jr) - 1u);
+  if (((unsigned)(st >> 32) & below) == 0u) return false;
+  const int64_t e0 = (pu0 - row * p.upr) * kUnitA;
+  const int64_t e1 = min((pu1 - row * p.upr) * kUnitA, (int64_t)p.V);
+  atomicAdd(p.skipped, (unsigned long long)((e1 - e0) * Elem<DT>::kSize));
+  return true;
+}
+
 // ---- the sequence outcome (verify) ------------------------------------------------------
 // State word of a sequence: bit i = position i accepted, bit 32 + i =
 // rejected (i < K <= 32).
@@ -1013,6 +1056,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       // the first round of row chunks is static (chunk = CTA): a CTA's first
       // copy does not wait behind every CTA's atomic on the counter
       unsigned long long next = blockIdx.x;
+      unsigned long long next_st = 0ull;  // its sequence's state (nothing decided yet)
       // Draw tickets.  At a piece boundary a producer that saw queued draws
       // nobody has taken claims a ticket (the first producer to reach a
       // boundary takes a new draw); a claimed ticket whose draw is not yet
@@ -1050,10 +1094,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           c = nS + (e - 1);
           ticket = -1;
         }
-        // 2. the next row chunk (its id was fetched one piece ago)
-        if (c < 0 && next < (unsigned long long)nS) {
-          c = (long long)next;
+        // 2. the next row chunk (its id and its sequence's state were fetched
+        //    one piece ago); a target row past a known rejection is dropped
+        while (c < 0 && next < (unsigned long long)nS) {
+          const long long cand = (long long)next;
+          const unsigned long long st = next_st;
           next = gridDim.x + atomicAdd(p.chunk_ctr, 1ull);
+          next_st = chunk_state(p, (long long)next, nS);
+          if (!chunk_past_rejection<DT>(p, cand, st)) c = cand;
         }
         // 3. nothing left to stream: wait for the draws still to come.  The
         //    producer leaves once every group is decided (no more draws can

@@ -241,6 +241,14 @@ def test_other_entry_points_reject_bad_arguments(L):
     assert L.ssd_cache_build_guesses(0x1000, 64, 0x2000, 2, 5, 3, None, None) == 3
     assert L.ssd_cache_lookup(None, 4096, 0x2000, 0x2000, 4, 0x3000, 0x4000, None) == 1
     assert L.ssd_cache_lookup(0x1000, 4096, 0x2000, 0x2000, 0, 0x3000, 0x4000, None) == 1
+    # (workspace, bytes, B, K, Kq, V, dtype, out, stream)
+    need = L.ssd_verify_workspace_size(4, 3, 4, 1000)
+    assert L.ssd_verify_skipped_bytes(0x1000, need, 4, 3, 4, 1000, 0, None, None) == 1
+    assert L.ssd_verify_skipped_bytes(0x1000, need, 4, 3, 5, 1000, 0, 0x2000, None) == 1
+    assert L.ssd_verify_skipped_bytes(0x1000, need, 4, 3, 4, 1000, 7, 0x2000, None) == 1
+    assert L.ssd_verify_skipped_bytes(None, need, 4, 3, 4, 1000, 0, 0x2000, None) == 5
+    assert L.ssd_verify_skipped_bytes(0x1008, need, 4, 3, 4, 1000, 0, 0x2000, None) == 5
+    assert L.ssd_verify_skipped_bytes(0x1000, need - 1, 4, 3, 4, 1000, 1, 0x2000, None) == 5
 
 
 def test_binding_fails_loudly_without_a_gpu():

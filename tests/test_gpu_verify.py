@@ -427,3 +427,34 @@ def test_gpu_laws_chi_square(orc):
         m = expect * len(sel) > 5
         st = stats.chisquare(obs[m], expect[m] / expect[m].sum() * obs[m].sum())
         assert st.pvalue > 1e-4, (i, st)
+
+
+def test_target_rows_past_a_rejection_are_not_read(orc):
+    """The bytes of target rows the round did not read: a multiple of the
+    element size, at most the target rows past position 0 of every rejected
+    sequence (rows past its first rejection), and some at the c5 shape, where
+    most sequences stop early; the outputs equal the oracle (every test of
+    this file runs with rows skipped)."""
+    torch, dev = torch_dev()
+    w = WORKLOADS["c5"]
+    B = 64
+    bt = make_batch(w, B=B, seed=21)
+    tg, dg = upload(bt["target"], "f32"), upload(bt["draft"], "f32")
+    F = np.asarray(w.fanout, dtype=np.int32)
+    tok = orc.draft_tokens(bt["draft"], F, w.C, w.T, bt["seeds"], K=w.K, nthreads=16)
+    ws = torch.zeros(ssd.lib().ssd_verify_workspace_size(B, w.K, w.Kq, w.V), dtype=torch.uint8,
+                     device=dev)
+    out = {}
+    total = 0
+    for rnd in range(4):
+        g = ssd.verify_round(tg, dg, i32(tok), seeds_t(bt["seeds"]), rnd, F, w.C, w.T,
+                             workspace=ws, out=out)
+        sk = ssd.verify_skipped_bytes(ws, tg, w.K, w.Kq)
+        al = g["accept_len"].cpu().numpy()
+        bound = int(np.where(al < w.K, w.K - al, 0).sum()) * w.V * 4
+        assert sk % 4 == 0 and 0 <= sk <= bound, (sk, bound)
+        total += sk
+        o = orc.verify(bt["target"], bt["draft"], tok, bt["seeds"], rnd, F, w.C, w.T, nthreads=16)
+        compare_verify(to_np({k: g[k] for k in ("accept_len", "bonus", "resid_mass", "guesses")}),
+                       o, w.K, V=w.V)
+    assert total > 0
