@@ -54,7 +54,7 @@ extern "C" {
 typedef enum {
   SSD_OK = 0,
   SSD_ERR_INVALID_ARG = 1,   /* an argument is out of range or inconsistent */
-  SSD_ERR_UNSUPPORTED = 2,   /* valid, but beyond this build's limits (e.g. F > 15) */
+  SSD_ERR_UNSUPPORTED = 2,   /* valid, but beyond the library's compiled limits (e.g. F > 15) */
   SSD_ERR_TABLE_FULL = 3,    /* host-detectable: cache capacity below 2 n */
   SSD_ERR_DUPLICATE_KEY = 4, /* reserved; duplicates are reported via dev_status */
   SSD_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or too small */
@@ -81,7 +81,7 @@ typedef struct {
   int64_t row_stride; /* elements between the starts of consecutive rows, >= V */
 } ssd_logits;
 
-/* Limits of this build. */
+/* Compiled limits of the library. */
 #define SSD_MAX_K 32       /* draft tokens per sequence */
 #define SSD_MAX_F 15       /* bonus guesses per position */
 #define SSD_MAX_V 16777215 /* vocabulary size (token ids and 24-bit uniforms stay exact) */
