@@ -70,6 +70,16 @@ def run_verify(orc, w, B=None, V=None, K=None, dtype=None, rounds=(0,), seed=Non
     return stats_all
 
 
+@pytest.mark.parametrize("T", [1.0, 0.0], ids=["sampled", "greedy"])
+def test_max_K_many_rows_with_rows_skipped(orc, T):
+    """K = 32 (the largest) over 600 sequences of small rows: with this many
+    rows every position streams after earlier positions are decided, so
+    target rows past a rejection are dropped at every position up to 32."""
+    w = dataclasses.replace(WORKLOADS["c1"], K=32)
+    st = run_verify(orc, w, B=600, V=256, K=32, F=[2] * 33, C=0.5, T=T, rounds=(0, 1))
+    assert sum(s["rows"] for s in st) == 1200
+
+
 def test_c1_tiny_exactness_many_rows(orc):
     """B=1,K=4,V=32 fp32 (C=0.5, F=[3,3,2,2,2]) drawn for 20000 independent
     sequences x 5 rounds."""
