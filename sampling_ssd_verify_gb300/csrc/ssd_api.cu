@@ -247,7 +247,7 @@ const char* ssd_status_string(int status) {
   switch (status) {
     case SSD_OK: return "ok";
     case SSD_ERR_INVALID_ARG: return "invalid argument";
-    case SSD_ERR_UNSUPPORTED: return "unsupported by this build";
+    case SSD_ERR_UNSUPPORTED: return "beyond the compiled limits of the library";
     case SSD_ERR_TABLE_FULL: return "cache table too small (capacity must be >= 2 n)";
     case SSD_ERR_DUPLICATE_KEY: return "duplicate cache key";
     case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
