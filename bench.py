@@ -57,6 +57,26 @@ def csrc_hash():
     return h.hexdigest()[:16]
 
 
+def verify_roofline(alg, skipped, launch_ms, launch_ms_median, hbm_peak, peak_kind, traffic):
+    """The roofline block of a verify round: `achieved` counts every logit once
+    (the algorithmic bytes) over the mean launch time; the bytes the round
+    actually streams (every logit minus the `skipped` target rows past a known
+    rejection) and their rate go beside it."""
+    read = alg - skipped
+    achieved = alg / (launch_ms * 1e-3) / 1e9
+    read_rate = read / (launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": traffic,
+            "kernel": "ssd_verify_round (streaming pass, bonus draws, outcome cache)",
+            "algorithmic_bytes_per_launch": alg,
+            "bytes_read_per_launch": read,
+            "skipped_target_bytes_per_launch": skipped,
+            "gb_per_s_on_bytes_read": read_rate,
+            "frac_on_bytes_read": read_rate / hbm_peak,
+            "launch_ms": launch_ms,
+            "launch_ms_median": launch_ms_median, "peak_kind": peak_kind}
+
+
 def traffic_from_profile(workload):
     """Per-launch DRAM bytes recorded by an ncu capture, if the kernels have
     not changed since (profiles/<...>.md carries 'csrc_sha: <hash>' and
@@ -232,26 +252,16 @@ def side_workload(name, steps, warmup, rank, dev, tdist):
         ssd.verify_round(tg, dg, tok, seeds, 5000 + s, F, w.C, w.T, table=table, workspace=ws,
                          out=out)
         skipped += ssd.verify_skipped_bytes(ws, tg, K, Kq)
-    streamed = alg - skipped / ns
     hbm_peak, peak_kind = peaks()
-    achieved = alg / (float(np.mean(launch)) * 1e-3) / 1e9
-    read_rate = streamed / (float(np.mean(launch)) * 1e-3) / 1e9
     world = tdist.get_world_size() if tdist.is_available() and tdist.is_initialized() else 1
     return {"workload": w.name, "B": B, "K": K, "Kq": Kq, "V": V, "dtype": w.dtype, "T": w.T,
             "C": w.C, "fanout": list(map(int, F)), "steps": steps, "warmup": warmup,
             "value": job_rows_per_s(B * steps, world, ms * 1e-3), "unit": "rows/s",
             "ms_per_step": ms / steps,
             "accept_mean": float(out["accept_len"].float().mean().item()),
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic_from_profile(name),
-                         "kernel": "ssd_verify_round (streaming pass, bonus draws, outcome cache)",
-                         "algorithmic_bytes_per_launch": alg,
-                         "bytes_read_per_launch": streamed,
-                         "skipped_target_bytes_per_launch": skipped / ns,
-                         "gb_per_s_on_bytes_read": read_rate,
-                         "frac_on_bytes_read": read_rate / hbm_peak,
-                         "launch_ms": float(np.mean(launch)),
-                         "launch_ms_median": float(np.median(launch)), "peak_kind": peak_kind},
+            "roofline": verify_roofline(alg, skipped / ns, float(np.mean(launch)),
+                                        float(np.median(launch)), hbm_peak, peak_kind,
+                                        traffic_from_profile(name)),
             "l2": "inputs larger than L2 (no flush)" if flush is None else
                   "inputs smaller than L2: a 256 MB write before each launch, outside its events"}
 
@@ -394,8 +404,6 @@ def run_ours(args):
     # logits minus those (measured on the same rounds); the roofline's
     # algorithmic bytes stay every logit once, the bytes read go beside them
     streamed = alg - skipped / nr
-    achieved = alg / (verify_ms * 1e-3) / 1e9
-    read_rate = streamed / (verify_ms * 1e-3) / 1e9
 
     # end to end through the public API with host buffers
     e2e = None
@@ -487,18 +495,9 @@ def run_ours(args):
                        "accept_mean": acc_sum / nr, "alpha_measured": alpha, "hit_rate": h,
                        "all_hit_fraction": all_hits / nr, "h_pow_B": h ** B,
                        "wall_s_timed": wall},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic,
-                         "kernel": "ssd_verify_round (streaming pass, bonus draws, outcome cache)",
-                         "algorithmic_bytes_per_launch": alg,
-                         "bytes_read_per_launch": streamed,
-                         "skipped_target_bytes_per_launch": skipped / nr,
-                         "gb_per_s_on_bytes_read": read_rate,
-                         "frac_on_bytes_read": read_rate / hbm_peak,
-                         "launch_ms": verify_ms,
-                         "launch_ms_median": verify_ms_median,
-                         "tail_bytes_per_launch": tail_bytes,
-                         "peak_kind": peak_kind},
+            "roofline": dict(verify_roofline(alg, skipped / nr, verify_ms, verify_ms_median,
+                                             hbm_peak, peak_kind, traffic),
+                             tail_bytes_per_launch=tail_bytes),
             "e2e": e2e,
             "workloads": sides or None,
             "gpu_launches": args.steps,

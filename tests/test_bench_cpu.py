@@ -54,3 +54,21 @@ def test_ranks_draw_different_batches():
     a = make_batch(w, B=1, V=256, seed=bench.rank_seed(w, 0))
     b = make_batch(w, B=1, V=256, seed=bench.rank_seed(w, 1))
     assert not np.array_equal(a["target"], b["target"])
+
+
+def test_roofline_counts_every_logit_and_reports_the_bytes_read_beside():
+    # 2.8 GB of logits, 0.96 GB of them not read, one launch of 0.4 ms, a
+    # 7000 GB/s peak: 7000 GB/s on every logit (frac 1.0), 4600 GB/s on the
+    # 1.84 GB read (frac 4600 / 7000)
+    r = bench.verify_roofline(2.8e9, 0.96e9, 0.4, 0.39, 7000.0, "measured", 2.3e9)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 7000.0
+    assert abs(r["achieved"] - 7000.0) < 1e-6 and abs(r["frac"] - 1.0) < 1e-12
+    assert abs(r["bytes_read_per_launch"] - 1.84e9) < 1.0
+    assert abs(r["gb_per_s_on_bytes_read"] - 4600.0) < 1e-6
+    assert abs(r["frac_on_bytes_read"] - 4600.0 / 7000.0) < 1e-12
+    assert r["algorithmic_bytes_per_launch"] == 2.8e9
+    assert r["skipped_target_bytes_per_launch"] == 0.96e9
+    assert r["traffic"] == 2.3e9 and r["launch_ms"] == 0.4 and r["launch_ms_median"] == 0.39
+    # nothing skipped: both fractions agree
+    r0 = bench.verify_roofline(1e9, 0.0, 1.0, 1.0, 1000.0, "fallback", None)
+    assert r0["frac"] == r0["frac_on_bytes_read"] == 1.0 and r0["traffic"] is None
