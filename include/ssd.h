@@ -361,7 +361,9 @@ ssd_status ssd_saguaro_sample(const ssd_logits* draft, int R, int V, float T, fl
  * T           temperature, finite and > 0.   N <= 256.
  * workspace   >= ssd_tree_workspace_size(B, N, V), 256-byte aligned.
  * Two launches on `stream`: the streaming pass normalises every row, then
- * one CTA per tree walks it.
+ * one thread-block cluster per tree walks it: its CTAs share the tree's row
+ * passes; 8 CTAs, halved while B times the cluster size exceeds the SM
+ * count (one CTA per tree when B does).
  * ------------------------------------------------------------------------- */
 size_t ssd_tree_workspace_size(int B, int N, int V);
 ssd_status ssd_tree_verify(const ssd_logits* target, const ssd_logits* draft, int B, int N, int V,
